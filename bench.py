@@ -1,0 +1,367 @@
+"""Benchmark: one Barnes-Hut force evaluation per step on synthetic Plummer spheres.
+
+A step is one whole evaluation through the C ABI (bounding cube, Morton keys,
+radix sort, gather, octree build, moments, coherent walk, scatter) with the
+inputs already resident in device memory. Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--traversal coherent|independent] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain C restatement of the
+method) on this host's cores instead, on a bounded sample of the same
+workload. Under torchrun (N > 1) every rank evaluates its own full problem on
+its own GPU (independent replicas, weak scaling); there is no collective on
+the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BH force-evaluation ms and interactions/s at N=1M on 1 GB300; % of FP32/HBM roofline"
+UNIT = "interactions/s"
+FLOPS_PER_INTERACTION = 18  # 3 FADD, 3 FFMA (x2), 1 FADD, 2+1 FMUL, 3 FFMA (x2) per term
+FLOPS_PER_VISIT = 9         # acceptance test: 3 FADD, 1 FMUL + 2 FFMA (x2), 1 FMUL
+FP32_LANES_PER_SM = 128
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=11)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--workload", default="plummer_1048576")
+    p.add_argument("--traversal", default="coherent", choices=["coherent", "independent"])
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=8.0,
+                   help="target wall time of the CPU-oracle sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+def profile_traffic(kernel_src: str) -> float | None:
+    """Per-launch DRAM bytes of the walk kernel from the committed ncu summary,
+    only while the kernel source is the one that was profiled."""
+    path = os.path.join(ROOT, "profiles", "walk_coherent_plummer_1m.md")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    found_sha, traffic = None, None
+    for line in open(path):
+        if line.startswith("kernel_source_sha256:"):
+            found_sha = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch_full_size:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if found_sha == sha else None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(pos, mass, params, seconds: float) -> dict:
+    """The oracle as it stands on this host's cores: full tree build plus the
+    walk of a sample of whole 32-target groups; scaled to interactions/s of a
+    whole evaluation (build + all targets)."""
+    import oracle
+
+    threads = oracle.default_threads()
+    n = pos.shape[0]
+    t0 = time.perf_counter()
+    T = oracle.Tree(pos, mass, params["leaf_cap"])
+    t_build = time.perf_counter() - t0
+    nw = (n + 31) // 32
+
+    def walk_every(stride):
+        warps = np.arange(0, nw, stride)
+        tgt = np.concatenate([np.arange(32 * w, min(n, 32 * w + 32)) for w in warps])
+        t0 = time.perf_counter()
+        _, pc, pp, _ = T.walk(params["theta"], params["eps"], tgt, threads=threads)
+        return tgt, pc, pp, time.perf_counter() - t0
+
+    # calibrate on every 512th group, then size the sample to the time budget
+    tgt, pc, pp, t_walk = walk_every(min(512, nw))
+    per_target = t_walk / len(tgt)
+    stride = int(max(1, min(nw, round(n * per_target / max(seconds, 1e-3)))))
+    if stride < min(512, nw):
+        tgt, pc, pp, t_walk = walk_every(stride)
+    inter_sample = float(pc.sum() + pp.sum())
+    t_full = t_build + t_walk * n / len(tgt)
+    inter_full = inter_sample * n / len(tgt)
+    import platform
+    return {"value": inter_full / t_full, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "full tree build (%.2f s, 1 thread) + walks of %d of %d targets in whole "
+                      "32-target groups (%.2f s, %d threads), scaled to all targets"
+                      % (t_build, len(tgt), n, t_walk, threads),
+            "ms_per_evaluation_est": 1000.0 * t_full, "cpu": platform.machine()}
+
+
+def run_reference(args, rank: int, world: int) -> None:
+    from inputs import workload
+
+    if rank != 0:
+        return
+    pos, mass, params = workload(args.workload)
+    times, vals = [], []
+    cb = None
+    for step in range(args.warmup + args.steps):
+        cb = cpu_baseline(pos, mass, params, min(args.cpu_seconds, 4.0))
+        if step >= args.warmup:
+            times.append(cb["ms_per_evaluation_est"])
+            vals.append(cb["value"])
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": statistics.median(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "n": int(pos.shape[0]), **params,
+                       "traversal": "independent (CPU oracle)"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+
+    import torch
+
+    import tree_traversal_gb300 as tt
+    from inputs import workload
+    from tree_traversal_gb300.build import build
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    if rank == 0:
+        build()
+    if dist is not None:
+        dist.barrier()
+    tt.load()
+
+    pos_np, mass_np, params = workload(args.workload)
+    n = pos_np.shape[0]
+    pos = torch.from_numpy(pos_np).to(device)
+    mass = torch.from_numpy(mass_np).to(device)
+    acc = torch.empty((n, 3), dtype=torch.float32, device=device)
+    inter = torch.empty((n, 2), dtype=torch.int32, device=device)
+    visits = torch.empty(n, dtype=torch.int32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    call = lambda trav: tt.bh_forces(pos, mass, params["theta"], params["eps"], params["leaf_cap"],
+                                     trav, out=(acc, inter, visits))
+
+    # untimed: the comparison traversal (its visits give the redundancy ratio)
+    other = "independent" if args.traversal == "coherent" else "coherent"
+    call(other)
+    t_other = tt.last_timings()
+    vis_other = visits.double().mean().item()
+    for _ in range(args.warmup):
+        call(args.traversal)
+    torch.cuda.synchronize(device)
+    interactions = float(inter.double().sum().item())
+    vis_mean = visits.double().mean().item()
+    pc_mean = inter[:, 0].double().mean().item()
+    pp_mean = inter[:, 1].double().mean().item()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    phases, step_ms = [], []
+    launches0 = tt.kernel_launches()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index) as clocks:
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            flush.zero_()  # evict L2 between steps (outside the step's events)
+            ev[s][0].record(stream)
+            call(args.traversal)
+            ev[s][1].record(stream)
+            phases.append(tt.last_timings())
+        torch.cuda.synchronize(device)
+        if dist is not None:
+            dist.barrier()
+        wall = time.perf_counter() - t0
+    launches = tt.kernel_launches() - launches0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * interactions / (ms_per_step / 1000.0)
+
+    def mean(key):
+        return statistics.fmean(p[key] for p in phases)
+
+    walk_ms = mean("walk_ms")
+    # the pages' independent walk gives the algorithmic count; the coherent
+    # walk's extra (union) visits are overhead, not work
+    vis_ind = vis_mean if args.traversal == "independent" else vis_other
+    flops_inter = FLOPS_PER_INTERACTION * interactions
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    peaks = measured_peaks()
+    clk = peaks.get("sm_max_mhz", 2070.0)
+    peak_tflops = sms * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12
+    achieved = flops_inter / (walk_ms / 1000.0) / 1e12
+    csum = clocks.summary()
+
+    # e2e: the host entry point, pinned buffers, copies inside the timed call
+    h_pos = torch.from_numpy(pos_np).pin_memory()
+    h_mass = torch.from_numpy(mass_np).pin_memory()
+    h_out = (torch.empty((n, 3)).pin_memory(), torch.empty((n, 2), dtype=torch.int32).pin_memory(),
+             torch.empty(n, dtype=torch.int32).pin_memory())
+    for _ in range(2):
+        tt.bh_forces_host(h_pos, h_mass, params["theta"], params["eps"], params["leaf_cap"],
+                          args.traversal, out=h_out, device=device)
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize(device)
+        t1 = time.perf_counter()
+        tt.bh_forces_host(h_pos, h_mass, params["theta"], params["eps"], params["leaf_cap"],
+                          args.traversal, out=h_out, device=device)
+        e2e_ms.append(1000.0 * (time.perf_counter() - t1))
+    e2e_host = tt.last_timings()
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    cb = None
+    if not args.no_cpu_baseline and world == 1:
+        cb = cpu_baseline(pos_np, mass_np, params, args.cpu_seconds)
+    walk_src = os.path.join(ROOT, "tree_traversal_gb300", "csrc", "bh_walk.cu")
+    traffic = profile_traffic(walk_src)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "n": n, "theta": params["theta"],
+                   "eps": params["eps"], "leaf_cap": params["leaf_cap"],
+                   "traversal": args.traversal, "parallelism": "replicas" if world > 1 else "1gpu",
+                   "l2": "flushed between steps (256 MiB write outside the step events)"},
+        "gpu_launches": int(launches),
+        "clocks": {"sm_mhz": csum["sm_mhz"], "sm_max_mhz": csum["sm_max_mhz"],
+                   "reasons": csum["reasons"]},
+        "roofline": {"bound": "alu", "kernel": "k_walk_coherent" if args.traversal == "coherent"
+                     else "k_walk_independent",
+                     "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tflops, "traffic": traffic,
+                     "peak_basis": "%d SMs x %d FP32 lanes x 2 flop x %.0f MHz (max SM clock of "
+                                   "measured peaks)" % (sms, FP32_LANES_PER_SM, clk),
+                     "flops_per_launch": flops_inter,
+                     "flops_per_interaction": FLOPS_PER_INTERACTION,
+                     "walk_ms": walk_ms,
+                     "frac_at_sampled_clock": (achieved / (peak_tflops * csum["sm_mhz"] / clk))
+                     if csum["sm_mhz"] else None,
+                     "frac_incl_acceptance": (flops_inter + FLOPS_PER_VISIT * vis_ind * n)
+                     / (walk_ms / 1000.0) / 1e12 / peak_tflops},
+        "cpu_baseline": None if cb is None else
+        {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": interactions / (statistics.median(e2e_ms) / 1000.0), "unit": UNIT,
+                "h2d_bytes_per_step": 16 * n, "d2h_bytes_per_step": 24 * n,
+                "ms_median": statistics.median(e2e_ms), "h2d_ms": e2e_host["h2d_ms"],
+                "d2h_ms": e2e_host["d2h_ms"]},
+        "phases_ms": {k: mean(k) for k in ("bbox_ms", "morton_ms", "sort_ms", "gather_ms",
+                                           "build_ms", "moments_ms", "walk_ms", "scatter_ms",
+                                           "total_ms")},
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms),
+                    "wall_s_incl_flush": wall},
+        "tree": {"num_nodes": phases[-1]["num_nodes"], "depth": phases[-1]["depth"]},
+        "per_particle": {"interactions": interactions / n, "cells": pc_mean, "particles": pp_mean,
+                         "visits": vis_mean, "visits_" + other: vis_other,
+                         "redundancy": (vis_mean / vis_other) if args.traversal == "coherent"
+                         else (vis_other / vis_mean)},
+        "walk_ms_" + other: t_other["walk_ms"],
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

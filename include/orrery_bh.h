@@ -1,0 +1,160 @@
+/*
+ * orrery_bh.h -- C ABI of the GB300 Barnes-Hut monopole force evaluation.
+ *
+ * One call evaluates softened gravitational accelerations for n particles with
+ * a stackless depth-first octree and escape indices, as the orrery pages
+ * describe it:
+ *   - "sycl_tree_solver.hpp" reference page, Detailed Description: the walk,
+ *     the gather into tree order and the scatter back to the caller's order,
+ *     and the TreeTraversal enumeration {kIndependent, kCoherent};
+ *   - "ADR-0029: Mask the accepted cells rather than descending together",
+ *     Decision: the coherent walk advances each warp to the smallest node
+ *     index any lane still wants, so every target is summed over exactly the
+ *     nodes its own walk visits, in the same order;
+ *   - "docs/performance/sycl_tree.md", "The machine and the device" table:
+ *     softening, opening angle, leaf capacity, monopole only; "The divergence
+ *     mitigation": what a node visit is.
+ *
+ * Arithmetic (both traversals, every step): IEEE binary32, round to nearest.
+ *   cube:      lo_a = min x_a; side = max_a (max x_a - lo_a); inv = 2^21 / side
+ *   key:       q_a = min(floor((x_a - lo_a) * inv), 2^21 - 1), bits of x, y, z
+ *              interleaved x-high into a 63-bit Morton key
+ *   sort:      stable on (key, original index)
+ *   tree:      a cell is split iff it holds more than leaf_cap particles and
+ *              its level is below 21; one child per non-empty octant, in
+ *              octant order; nodes in depth-first preorder
+ *   moments:   leaf M = sum m, S = sum fma(m, x, S) in sorted order; internal
+ *              nodes sum their children in order; CoM = S / M (0 if M <= 0)
+ *   criterion: accept iff (side 2^-L)^2 < (theta^2) * |CoM - x_i|^2
+ *   term:      r2 = |x_j - x_i|^2 + eps^2; f = m_j / (r2 sqrt(r2));
+ *              a_i += f (x_j - x_i), fused multiply-add, in walk order
+ * Both traversals give bit-identical accelerations and counters.
+ *
+ * Memory: every pointer named *_d or documented "device" is a CUDA device
+ * pointer on the current device, owned by the caller. The library owns a
+ * grow-only scratch workspace per device (released by orrery_bh_release).
+ * Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream); each call blocks once at its end to read back a status word.
+ * Calls are serialised by an internal lock; one call at a time per process.
+ *
+ * Errors: a negative status; on any non-zero status the outputs are undefined.
+ */
+#ifndef ORRERY_BH_H
+#define ORRERY_BH_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ORRERY_OK 0
+#define ORRERY_EINVAL (-1)     /* bad argument; nothing was launched */
+#define ORRERY_ENONFINITE (-2) /* a position or mass is NaN or infinite */
+#define ORRERY_ERANGE (-3)     /* node count or size beyond the int32 range */
+#define ORRERY_ECUDA (-4)      /* a CUDA runtime call failed */
+#define ORRERY_EWALK (-5)      /* a walk exceeded its iteration bound */
+#define ORRERY_ENOMEM (-6)     /* the workspace could not be allocated */
+#define ORRERY_EINTERNAL (-7)  /* an index failed a device-side consistency check;
+                                  the access was skipped (a library defect) */
+
+/* Which traversal the walk kernel runs ("sycl_tree_solver.hpp",
+ * TreeTraversal). Both compute the same function of the input. */
+typedef enum {
+    ORRERY_INDEPENDENT = 0, /* one thread per target, each on its own node index */
+    ORRERY_COHERENT = 1     /* one node index per warp, advanced by min over lanes */
+} orrery_traversal;
+
+/* Where the last evaluation spent its time ("sycl_tree_solver.hpp",
+ * SyclTreeTimings), measured with CUDA events on the call's stream. */
+typedef struct {
+    float h2d_ms;     /* orrery_bh_forces_host only: host-to-device copies */
+    float bbox_ms;    /* bounding cube reduction */
+    float morton_ms;  /* quantise + interleave */
+    float sort_ms;    /* radix sort of (key, index) */
+    float gather_ms;  /* particles into tree order */
+    float build_ms;   /* octree nodes and escape indices */
+    float moments_ms; /* upward mass / centre-of-mass pass */
+    float walk_ms;    /* the traversal */
+    float scatter_ms; /* results back to caller order */
+    float d2h_ms;     /* orrery_bh_forces_host only: device-to-host copies */
+    float total_ms;   /* first event to last */
+    int32_t traversal;
+    int32_t depth;       /* deepest node level */
+    int64_t n;
+    int64_t num_nodes;
+    uint64_t launches;   /* kernels launched by that call */
+} orrery_bh_timings;
+
+/*
+ * Evaluates accelerations for n particles.
+ *   pos_d        device, float32 [n][3] contiguous (x, y, z per particle)
+ *   mass_d       device, float32 [n]
+ *   n            0 <= n <= 2^30; n == 0 returns ORRERY_OK and launches nothing
+ *   theta        opening angle, >= 0 (0 opens every cell: direct summation)
+ *   eps          Plummer softening length, >= 0
+ *   leaf_cap     >= 1: a cell holding at most this many particles is a leaf
+ *   traversal    ORRERY_INDEPENDENT or ORRERY_COHERENT
+ *   acc_d        device, float32 [n][3], written in the caller's order
+ *   interactions_d  device, uint32 [n][2] {particle-cell, particle-particle}
+ *                per target in the caller's order, or NULL
+ *   visits_d     device, uint32 [n] node visits per target, or NULL. For the
+ *                independent walk a target's own walk; for the coherent walk
+ *                the size of its warp's union (32 consecutive sorted targets)
+ *   stream       cudaStream_t
+ * Returns ORRERY_OK or a negative status.
+ */
+int orrery_bh_forces(const float *pos_d, const float *mass_d, int64_t n, float theta, float eps,
+                     int32_t leaf_cap, int32_t traversal, float *acc_d, uint32_t *interactions_d,
+                     uint32_t *visits_d, void *stream);
+
+/*
+ * The same evaluation from and to HOST memory (page-locked memory gives the
+ * fastest copies; pageable memory works). The copies run on `stream` inside
+ * the call; pos, mass and acc are required, interactions and visits may be
+ * NULL. Shapes and order as in orrery_bh_forces.
+ */
+int orrery_bh_forces_host(const float *pos, const float *mass, int64_t n, float theta, float eps,
+                          int32_t leaf_cap, int32_t traversal, float *acc, uint32_t *interactions,
+                          uint32_t *visits, void *stream);
+
+/*
+ * Runs the cube, key, sort, gather, build and moments steps and copies their
+ * results out (for inspection and tests). Every output is a device pointer
+ * and may be NULL:
+ *   cube_d       float32 [5] {lo_x, lo_y, lo_z, side, inv}
+ *   keys_d       uint64 [n] Morton keys in sorted order
+ *   perm_d       uint32 [n] original index of each sorted slot
+ *   nodes_d      int32 [max_nodes][4] {escape, first, count, level}, preorder
+ *   com_d        float32 [max_nodes][4] {CoM_x, CoM_y, CoM_z, M}
+ *   num_nodes    host int64, the node count (required)
+ * Returns ORRERY_ERANGE when max_nodes is below the node count (num_nodes is
+ * still set).
+ */
+int orrery_bh_tree(const float *pos_d, const float *mass_d, int64_t n, int32_t leaf_cap,
+                   float *cube_d, uint64_t *keys_d, uint32_t *perm_d, int32_t *nodes_d,
+                   float *com_d, int64_t max_nodes, int64_t *num_nodes, void *stream);
+
+/* Upper bound of the node count for n particles and a leaf capacity:
+ * n + 21 * floor(n / (leaf_cap + 1)) + 1 (leaves are disjoint and non-empty;
+ * internal cells of one level are disjoint and hold more than leaf_cap).
+ * Returns -1 for invalid arguments. */
+int64_t orrery_bh_max_nodes(int64_t n, int32_t leaf_cap);
+
+/* Copies the phase timings of the last successful evaluation on this process. */
+int orrery_bh_last_timings(orrery_bh_timings *out);
+
+/* Total kernels this library has launched in this process. */
+uint64_t orrery_bh_kernel_launches(void);
+
+/* A static string describing a status code. */
+const char *orrery_bh_strerror(int status);
+
+/* Frees the workspaces of every device this process used. */
+void orrery_bh_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ORRERY_BH_H */

@@ -1,0 +1,272 @@
+"""GPU parity: the sm_103a library against the CPU oracle, through the C ABI.
+
+Bars (the oracle and the kernels take every decision and sum in the same
+binary32 operations, in the same order):
+  * cube, sorted keys, permutation, node records: bit-exact;
+  * node moments (CoM, M): bit-exact;
+  * interaction counts and visit counts: bit-exact (coherent visits against
+    the oracle's union of the 32 lanes' walks);
+  * accelerations: bit-exact, and in any case within 1e-5 max relative error
+    (the stated tolerance);
+  * the coherent and the independent walk: bit-identical to each other.
+Sizes span several radix tiles (4096 keys) and scan tiles (2048 entries) with
+ragged tails; the full-size workloads (1M Plummer, two 1M spheres swept over
+theta) are compared over the whole tree and on sampled warps of targets.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from inputs import PAGES_SEED, plummer, two_spheres, uniform_cube
+
+pytestmark = pytest.mark.gpu
+EPS = 0.05
+REL_TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def tt():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tree_traversal_gb300.build import build
+
+    build()
+    import tree_traversal_gb300 as tt
+
+    tt.load()
+    return tt
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def _dup():
+    p = np.zeros((105, 3), np.float32)
+    p[:65] = 0.25
+    p[65:] = uniform_cube(40, 9)[0]
+    return p, np.full(105, 1 / 105, np.float32), 32
+
+
+def _clump():
+    c, _ = uniform_cube(300, 4, 0.0, 1e-4)
+    p = np.concatenate([c, uniform_cube(60, 5)[0]]).astype(np.float32)
+    return p, np.full(len(p), 1 / len(p), np.float32), 8
+
+
+def _grid():
+    g = np.stack(np.meshgrid(*[np.arange(12)] * 3, indexing="ij"), -1).reshape(-1, 3)
+    p = np.concatenate([g, g[::7]]).astype(np.float32)  # exact ties on keys
+    return p, np.full(len(p), 1 / len(p), np.float32), 4
+
+
+def _masses(n, seed):
+    pos, _ = plummer(n, seed)
+    m = np.random.default_rng(seed).uniform(0.1, 2.0, n).astype(np.float32) / n
+    return pos, m, 16
+
+
+CASES = {
+    "plummer_4096": lambda: (*plummer(4096), 32),
+    "plummer_16384": lambda: (*plummer(16384), 32),
+    "plummer_131072": lambda: (*plummer(131072), 32),
+    "ragged_5003_cap7": lambda: (*plummer(5003, 77), 7),
+    "ragged_4097_cap32": lambda: (*plummer(4097, 78), 32),
+    "tiny_33_cap1": lambda: (*uniform_cube(33, 5), 1),
+    "single": lambda: (np.array([[1.0, 2.0, 3.0]], np.float32), np.array([0.5], np.float32), 32),
+    "pair_coincident": lambda: (np.full((2, 3), 0.5, np.float32), np.full(2, 0.5, np.float32), 32),
+    "duplicates_65": _dup,
+    "clump_cap8": _clump,
+    "grid_ties_cap4": _grid,
+    "unequal_masses_cap16": lambda: _masses(9000, 12),
+    "uniform_20000_cap200": lambda: (*uniform_cube(20000, 6), 200),
+    "two_spheres_2x8192": lambda: (*two_spheres(8192), 32),
+}
+_cache = {}
+
+
+def case(name):
+    if name not in _cache:
+        pos, mass, cap = CASES[name]()
+        _cache[name] = (pos, mass, cap, oracle.Tree(pos, mass, cap))
+    return _cache[name]
+
+
+def check_tree(tt, pos, mass, cap, T):
+    g = tt.bh_tree(dev(pos), dev(mass), cap)
+    cube = g["cube"].cpu().numpy()
+    assert np.array_equal(cube[:3], T.lo) and cube[3] == T.side and cube[4] == T.inv
+    assert np.array_equal(g["keys"].cpu().numpy().view(np.uint64), T.sorted_keys)
+    assert np.array_equal(u32(g["perm"]), T.perm)
+    assert np.array_equal(g["nodes"].cpu().numpy(), T.nodes)
+    assert np.array_equal(g["com"].cpu().numpy().view(np.uint32), T.cm.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_tree_bit_exact(tt, name):
+    pos, mass, cap, T = case(name)
+    check_tree(tt, pos, mass, cap, T)
+
+
+def check_forces(tt, pos, mass, cap, T, theta, traversal):
+    acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), theta, EPS, cap, traversal)
+    r_acc, r_pc, r_pp, r_vis = T.walk(theta, EPS, threads=oracle.default_threads())
+    inv = T.perm  # caller index of each sorted slot
+    g_acc = acc.cpu().numpy()[inv]
+    assert oracle.relative_error(g_acc, r_acc).max() <= REL_TOL or np.array_equal(g_acc, r_acc)
+    assert np.array_equal(g_acc.view(np.uint32), r_acc.view(np.uint32))
+    g_inter = u32(inter)[inv]
+    assert np.array_equal(g_inter[:, 0], r_pc) and np.array_equal(g_inter[:, 1], r_pp)
+    if traversal == "independent":
+        want = r_vis
+    else:
+        want = np.repeat(T.group_visits(theta, EPS, 32), 32)[: T.n]
+    assert np.array_equal(u32(vis)[inv], want)
+    t = tt.last_timings()
+    assert t["num_nodes"] == T.num_nodes and t["depth"] == T.depth and t["n"] == T.n
+
+
+@pytest.mark.parametrize("traversal", ["coherent", "independent"])
+@pytest.mark.parametrize("name", list(CASES))
+def test_forces_bit_exact(tt, name, traversal):
+    pos, mass, cap, T = case(name)
+    check_forces(tt, pos, mass, cap, T, 0.5, traversal)
+
+
+@pytest.mark.parametrize("theta", [0.0, 0.3, 0.7, 1.0, 1e30])
+@pytest.mark.parametrize("name", ["ragged_5003_cap7", "duplicates_65", "grid_ties_cap4"])
+def test_forces_theta_sweep(tt, name, theta):
+    pos, mass, cap, T = case(name)
+    for traversal in ("coherent", "independent"):
+        check_forces(tt, pos, mass, cap, T, theta, traversal)
+
+
+def test_empty_input(tt):
+    acc, inter, vis = tt.bh_forces(torch.zeros((0, 3), device="cuda"), torch.zeros(0, device="cuda"))
+    assert acc.shape == (0, 3)
+
+
+def test_nonfinite_input_is_reported(tt):
+    pos, mass = plummer(3000, 1)
+    for bad in ("pos", "mass"):
+        p, m = pos.copy(), mass.copy()
+        if bad == "pos":
+            p[1234, 1] = np.nan
+        else:
+            m[17] = np.inf
+        with pytest.raises(tt.OrreryError) as e:
+            tt.bh_forces(dev(p), dev(m))
+        assert e.value.status == -2
+    # the library recovers: the next valid call is exact again
+    pos, mass, cap, T = case("plummer_4096")
+    check_forces(tt, pos, mass, cap, T, 0.5, "coherent")
+
+
+def test_invalid_arguments_raise(tt):
+    pos, mass = dev(plummer(100, 1)[0]), dev(plummer(100, 1)[1])
+    with pytest.raises(tt.OrreryError):
+        tt.bh_forces(pos, mass, theta=-1.0)
+    with pytest.raises(tt.OrreryError):
+        tt.bh_forces(pos, mass, leaf_cap=0)
+    with pytest.raises(ValueError):
+        tt.bh_forces(pos, mass, traversal="sideways")
+    with pytest.raises(ValueError):
+        tt.bh_forces(pos.cpu(), mass)
+
+
+def test_host_entry_point_matches_device(tt):
+    pos, mass, cap, T = case("ragged_5003_cap7")
+    acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), 0.5, EPS, cap, "coherent")
+    h_pos = torch.from_numpy(pos).pin_memory()
+    h_mass = torch.from_numpy(mass).pin_memory()
+    out = (torch.empty((T.n, 3)).pin_memory(), torch.empty((T.n, 2), dtype=torch.int32).pin_memory(),
+           torch.empty(T.n, dtype=torch.int32).pin_memory())
+    tt.bh_forces_host(h_pos, h_mass, 0.5, EPS, cap, "coherent", out=out)
+    assert np.array_equal(out[0].numpy().view(np.uint32), acc.cpu().numpy().view(np.uint32))
+    assert np.array_equal(out[1].numpy(), inter.cpu().numpy())
+    assert np.array_equal(out[2].numpy(), vis.cpu().numpy())
+    t = tt.last_timings()
+    assert t["h2d_ms"] >= 0 and t["d2h_ms"] >= 0 and t["total_ms"] >= t["walk_ms"]
+    # pageable numpy buffers work too
+    a2, i2, v2 = tt.bh_forces_host(pos, mass, 0.5, EPS, cap, "coherent")
+    assert np.array_equal(a2.view(np.uint32), acc.cpu().numpy().view(np.uint32))
+
+
+def test_repeatable_and_stream_local(tt):
+    pos, mass, cap, T = case("plummer_16384")
+    p, m = dev(pos), dev(mass)
+    a1, i1, v1 = tt.bh_forces(p, m, 0.5, EPS, cap)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a2, i2, v2 = tt.bh_forces(p, m, 0.5, EPS, cap)
+    s.synchronize()
+    assert torch.equal(a1, a2) and torch.equal(i1, i2) and torch.equal(v1, v2)
+    # counters off: same accelerations
+    a3, i3, v3 = tt.bh_forces(p, m, 0.5, EPS, cap, counters=False)
+    assert i3 is None and v3 is None and torch.equal(a1, a3)
+    # a smaller call after a larger one reuses the workspace correctly
+    pos2, mass2, cap2, T2 = case("ragged_4097_cap32")
+    check_forces(tt, pos2, mass2, cap2, T2, 0.5, "coherent")
+
+
+def test_timings_and_launch_count(tt):
+    pos, mass, cap, T = case("plummer_16384")
+    before = tt.kernel_launches()
+    tt.bh_forces(dev(pos), dev(mass), 0.5, EPS, cap)
+    t = tt.last_timings()
+    assert tt.kernel_launches() - before == t["launches"] > 0
+    phases = ["bbox_ms", "morton_ms", "sort_ms", "gather_ms", "build_ms", "moments_ms", "walk_ms",
+              "scatter_ms"]
+    assert all(t[k] >= 0 for k in phases)
+    assert abs(sum(t[k] for k in phases) - t["total_ms"]) <= 0.05 * t["total_ms"] + 0.05
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: whole-tree bit-exactness, sampled warps of targets
+# ---------------------------------------------------------------------------
+def sampled_warps(n, count=96):
+    nw = (n + 31) // 32
+    w = np.unique(np.concatenate([np.linspace(0, nw - 1, count).astype(np.int64), [0, nw - 1]]))
+    return w
+
+
+def check_full_size(tt, pos, mass, thetas, cap=32):
+    T = oracle.Tree(pos, mass, cap)
+    check_tree(tt, pos, mass, cap, T)
+    p, m = dev(pos), dev(mass)
+    warps = sampled_warps(T.n)
+    tgt = np.concatenate([np.arange(32 * w, min(T.n, 32 * w + 32)) for w in warps])
+    caller = T.perm[tgt]
+    for theta in thetas:
+        acc, inter, vis = tt.bh_forces(p, m, theta, EPS, cap, "coherent")
+        a_ind, i_ind, v_ind = tt.bh_forces(p, m, theta, EPS, cap, "independent")
+        # the two traversals agree everywhere, bit for bit
+        assert torch.equal(acc.view(torch.int32), a_ind.view(torch.int32))
+        assert torch.equal(inter, i_ind)
+        assert bool((vis >= v_ind).all())
+        r_acc, r_pc, r_pp, r_vis = T.walk(theta, EPS, tgt, threads=oracle.default_threads())
+        g_acc = acc.cpu().numpy()[caller]
+        assert oracle.relative_error(g_acc, r_acc).max() <= REL_TOL
+        assert np.array_equal(g_acc.view(np.uint32), r_acc.view(np.uint32))
+        g_inter = u32(inter)[caller]
+        assert np.array_equal(g_inter[:, 0], r_pc) and np.array_equal(g_inter[:, 1], r_pp)
+        assert np.array_equal(u32(v_ind)[caller], r_vis)
+        union = T.group_visits(theta, EPS, 32, warps)
+        assert np.array_equal(u32(vis)[caller], np.repeat(union, [min(32, T.n - 32 * w) for w in warps]))
+
+
+def test_full_size_plummer_1m(tt):
+    pos, mass = plummer(1048576, PAGES_SEED)
+    check_full_size(tt, pos, mass, [0.5])
+
+
+def test_full_size_two_spheres_theta_sweep(tt):
+    pos, mass = two_spheres(1048576)
+    check_full_size(tt, pos, mass, [0.3, 0.5, 0.7])

@@ -1,0 +1,423 @@
+// bh_api.cu -- the C ABI (include/orrery_bh.h): argument checks, the
+// per-device grow-only workspace, phase events, and the one blocking
+// read-back of the status word at the end of each call.
+//
+// The phase order follows the pages' force evaluation ("sycl_tree_solver.hpp",
+// SyclTreeTimings and "Where the tree comes from"; docs/performance/
+// sycl_tree.md, "Where one evaluation goes"): sort, gather, build, node
+// staging, walk, scatter. Here every phase runs on the device; the node
+// staging step has no counterpart because the build writes the walk's node
+// format directly, and the int32 bounds check it carried moves to the
+// argument checks below (node count bound against INT32_MAX).
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/orrery_bh.h"
+#include "bh_common.cuh"
+
+namespace obh {
+namespace {
+
+constexpr int64_t kMaxN = int64_t(1) << 30;
+constexpr int kMaxDevices = 64;
+
+enum Ev {
+    EV_H2D0,
+    EV_START,
+    EV_BBOX,
+    EV_MORTON,
+    EV_SORT,
+    EV_GATHER,
+    EV_BUILD,
+    EV_MOMENTS,
+    EV_WALK,
+    EV_SCATTER,
+    EV_D2H,
+    EV_COUNT
+};
+
+struct Workspace {
+    int device = -1;
+    void *base = nullptr;
+    size_t bytes = 0;
+    int64_t cap_n = -1;
+    int64_t cap_nodes = -1;
+    Buffers b{};
+    DeviceParams *host_params = nullptr;  // page-locked read-back slot
+    cudaEvent_t ev[EV_COUNT] = {};
+    // device staging for orrery_bh_forces_host
+    void *io = nullptr;
+    int64_t io_n = -1;
+};
+
+std::mutex g_mu;
+Workspace *g_ws[kMaxDevices] = {};
+orrery_bh_timings g_last{};
+bool g_have_last = false;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int64_t node_bound(int64_t n, int32_t cap)
+{
+    return n + 21 * (n / ((int64_t)cap + 1)) + 1;
+}
+
+int bbox_blocks_for(int64_t n)
+{
+    int64_t b = (n + 255) / 256;
+    if (b > 1216) b = 1216;  // 8 blocks per SM on 152 SMs
+    return (int)(b < 1 ? 1 : b);
+}
+
+// Lays the buffers of (n, nodes) out over one allocation; returns its size.
+size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
+{
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char * {
+        char *p = base ? base + off : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    b.n = n;
+    b.max_nodes = nodes;
+    b.radix_blocks = radix_blocks_for(n);
+    b.bbox_blocks = bbox_blocks_for(n);
+    const size_t n1 = (size_t)n + 1;
+    b.bbox_partial = (float *)take(sizeof(float) * 8 * (size_t)b.bbox_blocks);
+    b.params = (DeviceParams *)take(sizeof(DeviceParams));
+    b.keys_a = (uint64_t *)take(sizeof(uint64_t) * (size_t)n);
+    b.keys_b = (uint64_t *)take(sizeof(uint64_t) * (size_t)n);
+    b.idx_a = (uint32_t *)take(sizeof(uint32_t) * (size_t)n);
+    b.idx_b = (uint32_t *)take(sizeof(uint32_t) * (size_t)n);
+    b.radix_hist = (uint32_t *)take(sizeof(uint32_t) * 256 * (size_t)b.radix_blocks);
+    b.radix_total = (uint32_t *)take(sizeof(uint32_t) * 256);
+    b.ps = (float4 *)take(sizeof(float4) * (size_t)n);
+    b.lev_d = (int8_t *)take(n1);
+    b.lev_w = (int8_t *)take(n1);
+    b.ncount = (uint8_t *)take(n1);
+    b.pstart = (int32_t *)take(sizeof(int32_t) * n1);
+    b.node_start = (uint32_t *)take(sizeof(uint32_t) * n1);
+    b.scan_partial = (uint32_t *)take(sizeof(uint32_t) * (size_t)scan_partial_count((int64_t)n1));
+    b.meta = (int4 *)take(sizeof(int4) * (size_t)nodes);
+    b.parent = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
+    b.nchild = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
+    b.arrive = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
+    b.sums = (float4 *)take(sizeof(float4) * (size_t)nodes);
+    b.com = (float4 *)take(sizeof(float4) * (size_t)nodes);
+    b.acc_s = (float *)take(sizeof(float) * 3 * (size_t)n);
+    b.cnt_s = (uint32_t *)take(sizeof(uint32_t) * 3 * (size_t)n);
+    return off;
+}
+
+void free_workspace(Workspace *w)
+{
+    if (!w) return;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    cudaSetDevice(w->device);
+    if (w->base) cudaFree(w->base);
+    if (w->io) cudaFree(w->io);
+    if (w->host_params) cudaFreeHost(w->host_params);
+    for (int e = 0; e < EV_COUNT; ++e)
+        if (w->ev[e]) cudaEventDestroy(w->ev[e]);
+    if (prev >= 0) cudaSetDevice(prev);
+    delete w;
+}
+
+// The calling thread's current device's workspace, grown to (n, nodes).
+int get_workspace(int64_t n, int64_t nodes, Workspace **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ORRERY_ECUDA;
+    Workspace *w = g_ws[dev];
+    if (!w) {
+        w = new Workspace();
+        w->device = dev;
+        for (int e = 0; e < EV_COUNT; ++e)
+            if (cudaEventCreate(&w->ev[e]) != cudaSuccess) {
+                free_workspace(w);
+                return ORRERY_ECUDA;
+            }
+        if (cudaMallocHost((void **)&w->host_params, sizeof(DeviceParams)) != cudaSuccess) {
+            free_workspace(w);
+            return ORRERY_ENOMEM;
+        }
+        g_ws[dev] = w;
+    }
+    if (n > w->cap_n || nodes > w->cap_nodes) {
+        const int64_t cn = n > w->cap_n ? n : w->cap_n;
+        const int64_t cm = nodes > w->cap_nodes ? nodes : w->cap_nodes;
+        if (w->base) cudaFree(w->base);
+        w->base = nullptr;
+        w->cap_n = w->cap_nodes = -1;
+        Buffers probe{};
+        size_t bytes = carve(probe, nullptr, cn, cm);
+        if (cudaMalloc(&w->base, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            w->base = nullptr;
+            return ORRERY_ENOMEM;
+        }
+        w->bytes = bytes;
+        w->cap_n = cn;
+        w->cap_nodes = cm;
+    }
+    carve(w->b, (char *)w->base, n, nodes);
+    *out = w;
+    return ORRERY_OK;
+}
+
+int check_args(int64_t n, float theta, float eps, int32_t leaf_cap, int32_t traversal)
+{
+    if (n < 0 || n > kMaxN) return ORRERY_EINVAL;
+    if (!(theta >= 0.0f) || !(eps >= 0.0f)) return ORRERY_EINVAL;  // also rejects NaN
+    if (leaf_cap < 1) return ORRERY_EINVAL;
+    if (traversal != ORRERY_INDEPENDENT && traversal != ORRERY_COHERENT) return ORRERY_EINVAL;
+    if (node_bound(n, leaf_cap) > (int64_t)INT32_MAX) return ORRERY_ERANGE;
+    return ORRERY_OK;
+}
+
+float ms_between(cudaEvent_t a, cudaEvent_t b)
+{
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) {
+        cudaGetLastError();
+        return -1.0f;
+    }
+    return ms;
+}
+
+// Phases a1..a6 (through the moments). Returns the sorted keys / perm.
+void run_tree(Workspace &w, const float *pos, const float *mass, int32_t cap, cudaStream_t st,
+              uint64_t **keys_sorted, uint32_t **perm)
+{
+    const Buffers &b = w.b;
+    cudaEventRecord(w.ev[EV_START], st);
+    launch_bbox(pos, mass, b, st);
+    cudaEventRecord(w.ev[EV_BBOX], st);
+    launch_morton(pos, b, st);
+    cudaEventRecord(w.ev[EV_MORTON], st);
+    launch_sort(b, st, keys_sorted, perm);
+    cudaEventRecord(w.ev[EV_SORT], st);
+    launch_gather(pos, mass, *perm, b, st);
+    cudaEventRecord(w.ev[EV_GATHER], st);
+    launch_build(*keys_sorted, cap, b, st);
+    cudaEventRecord(w.ev[EV_BUILD], st);
+    launch_moments(cap, b, st);
+    cudaEventRecord(w.ev[EV_MOMENTS], st);
+}
+
+int finish(Workspace &w, cudaStream_t st)
+{
+    cudaMemcpyAsync(w.host_params, w.b.params, sizeof(DeviceParams), cudaMemcpyDeviceToHost, st);
+    if (cudaStreamSynchronize(st) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+        return ORRERY_ECUDA;
+    const int s = w.host_params->status;
+    if (s & kStatusNonFinite) return ORRERY_ENONFINITE;
+    if (s & kStatusNodeBound) return ORRERY_ERANGE;
+    if (s & kStatusWalkBound) return ORRERY_EWALK;
+    if (s & kStatusInternal) return ORRERY_EINTERNAL;
+    return ORRERY_OK;
+}
+
+// Enqueues phases a1..a8 and, for the host entry point, the result copies;
+// then blocks once and records the phase timings.
+struct HostOut {
+    float *acc;
+    uint32_t *inter;
+    uint32_t *visits;
+};
+
+int forces_device(Workspace &w, const float *pos, const float *mass, int64_t n, float theta,
+                  float eps, int32_t cap, int32_t traversal, float *acc, uint32_t *inter,
+                  uint32_t *visits, cudaStream_t st, const HostOut *host)
+{
+    const uint64_t launches0 = g_launches.load();
+    uint64_t *keys_sorted = nullptr;
+    uint32_t *perm = nullptr;
+    run_tree(w, pos, mass, cap, st, &keys_sorted, &perm);
+    launch_walk(traversal, theta, eps, cap, inter != nullptr || visits != nullptr, w.b, st);
+    cudaEventRecord(w.ev[EV_WALK], st);
+    launch_scatter(perm, w.b, acc, inter, visits, st);
+    cudaEventRecord(w.ev[EV_SCATTER], st);
+    if (host) {
+        cudaMemcpyAsync(host->acc, acc, 12 * (size_t)n, cudaMemcpyDeviceToHost, st);
+        if (host->inter)
+            cudaMemcpyAsync(host->inter, inter, 8 * (size_t)n, cudaMemcpyDeviceToHost, st);
+        if (host->visits)
+            cudaMemcpyAsync(host->visits, visits, 4 * (size_t)n, cudaMemcpyDeviceToHost, st);
+        cudaEventRecord(w.ev[EV_D2H], st);
+    }
+    const int rc = finish(w, st);
+    if (rc != ORRERY_OK) return rc;
+    orrery_bh_timings t{};
+    t.bbox_ms = ms_between(w.ev[EV_START], w.ev[EV_BBOX]);
+    t.morton_ms = ms_between(w.ev[EV_BBOX], w.ev[EV_MORTON]);
+    t.sort_ms = ms_between(w.ev[EV_MORTON], w.ev[EV_SORT]);
+    t.gather_ms = ms_between(w.ev[EV_SORT], w.ev[EV_GATHER]);
+    t.build_ms = ms_between(w.ev[EV_GATHER], w.ev[EV_BUILD]);
+    t.moments_ms = ms_between(w.ev[EV_BUILD], w.ev[EV_MOMENTS]);
+    t.walk_ms = ms_between(w.ev[EV_MOMENTS], w.ev[EV_WALK]);
+    t.scatter_ms = ms_between(w.ev[EV_WALK], w.ev[EV_SCATTER]);
+    t.total_ms = ms_between(w.ev[EV_START], w.ev[EV_SCATTER]);
+    if (host) {
+        t.h2d_ms = ms_between(w.ev[EV_H2D0], w.ev[EV_START]);
+        t.d2h_ms = ms_between(w.ev[EV_SCATTER], w.ev[EV_D2H]);
+        t.total_ms = ms_between(w.ev[EV_H2D0], w.ev[EV_D2H]);
+    }
+    t.traversal = traversal;
+    t.depth = w.host_params->depth;
+    t.n = n;
+    t.num_nodes = w.host_params->num_nodes;
+    t.launches = g_launches.load() - launches0;
+    g_last = t;
+    g_have_last = true;
+    return ORRERY_OK;
+}
+
+}  // namespace
+}  // namespace obh
+
+using namespace obh;
+
+extern "C" {
+
+int orrery_bh_forces(const float *pos_d, const float *mass_d, int64_t n, float theta, float eps,
+                     int32_t leaf_cap, int32_t traversal, float *acc_d, uint32_t *interactions_d,
+                     uint32_t *visits_d, void *stream)
+{
+    int rc = check_args(n, theta, eps, leaf_cap, traversal);
+    if (rc != ORRERY_OK) return rc;
+    if (n == 0) return ORRERY_OK;
+    if (!pos_d || !mass_d || !acc_d) return ORRERY_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace *w = nullptr;
+    rc = get_workspace(n, node_bound(n, leaf_cap), &w);
+    if (rc != ORRERY_OK) return rc;
+    return forces_device(*w, pos_d, mass_d, n, theta, eps, leaf_cap, traversal, acc_d,
+                         interactions_d, visits_d, (cudaStream_t)stream, nullptr);
+}
+
+int orrery_bh_forces_host(const float *pos, const float *mass, int64_t n, float theta, float eps,
+                          int32_t leaf_cap, int32_t traversal, float *acc, uint32_t *interactions,
+                          uint32_t *visits, void *stream)
+{
+    int rc = check_args(n, theta, eps, leaf_cap, traversal);
+    if (rc != ORRERY_OK) return rc;
+    if (n == 0) return ORRERY_OK;
+    if (!pos || !mass || !acc) return ORRERY_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace *w = nullptr;
+    rc = get_workspace(n, node_bound(n, leaf_cap), &w);
+    if (rc != ORRERY_OK) return rc;
+    // device staging: pos [3n] | mass [n] | acc [3n] | inter [2n] | visits [n]
+    if (n > w->io_n) {
+        if (w->io) cudaFree(w->io);
+        w->io = nullptr;
+        w->io_n = -1;
+        if (cudaMalloc(&w->io, align256(12 * (size_t)n) * 2 + align256(4 * (size_t)n) * 2 +
+                                   align256(8 * (size_t)n)) != cudaSuccess) {
+            cudaGetLastError();
+            w->io = nullptr;
+            return ORRERY_ENOMEM;
+        }
+        w->io_n = n;
+    }
+    char *p = (char *)w->io;
+    float *pos_d = (float *)p;
+    p += align256(12 * (size_t)w->io_n);
+    float *mass_d = (float *)p;
+    p += align256(4 * (size_t)w->io_n);
+    float *acc_d = (float *)p;
+    p += align256(12 * (size_t)w->io_n);
+    uint32_t *inter_d = (uint32_t *)p;
+    p += align256(8 * (size_t)w->io_n);
+    uint32_t *vis_d = (uint32_t *)p;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaEventRecord(w->ev[EV_H2D0], st);
+    cudaMemcpyAsync(pos_d, pos, 12 * (size_t)n, cudaMemcpyHostToDevice, st);
+    cudaMemcpyAsync(mass_d, mass, 4 * (size_t)n, cudaMemcpyHostToDevice, st);
+    const HostOut host{acc, interactions, visits};
+    return forces_device(*w, pos_d, mass_d, n, theta, eps, leaf_cap, traversal, acc_d,
+                         interactions ? inter_d : nullptr, visits ? vis_d : nullptr, st, &host);
+}
+
+int orrery_bh_tree(const float *pos_d, const float *mass_d, int64_t n, int32_t leaf_cap,
+                   float *cube_d, uint64_t *keys_d, uint32_t *perm_d, int32_t *nodes_d,
+                   float *com_d, int64_t max_nodes, int64_t *num_nodes, void *stream)
+{
+    int rc = check_args(n, 0.0f, 0.0f, leaf_cap, ORRERY_COHERENT);
+    if (rc != ORRERY_OK) return rc;
+    if (!num_nodes || max_nodes < 0) return ORRERY_EINVAL;
+    *num_nodes = 0;
+    if (n == 0) return ORRERY_OK;
+    if (!pos_d || !mass_d) return ORRERY_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace *w = nullptr;
+    rc = get_workspace(n, node_bound(n, leaf_cap), &w);
+    if (rc != ORRERY_OK) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint64_t *keys_sorted = nullptr;
+    uint32_t *perm = nullptr;
+    run_tree(*w, pos_d, mass_d, leaf_cap, st, &keys_sorted, &perm);
+    rc = finish(*w, st);
+    if (rc != ORRERY_OK) return rc;
+    const int64_t nn = w->host_params->num_nodes;
+    *num_nodes = nn;
+    if (cube_d) cudaMemcpyAsync(cube_d, w->b.params, 5 * sizeof(float), cudaMemcpyDeviceToDevice, st);
+    if (keys_d) cudaMemcpyAsync(keys_d, keys_sorted, 8 * (size_t)n, cudaMemcpyDeviceToDevice, st);
+    if (perm_d) cudaMemcpyAsync(perm_d, perm, 4 * (size_t)n, cudaMemcpyDeviceToDevice, st);
+    const int64_t nc = nn < max_nodes ? nn : max_nodes;
+    if (nodes_d && nc > 0)
+        cudaMemcpyAsync(nodes_d, w->b.meta, 16 * (size_t)nc, cudaMemcpyDeviceToDevice, st);
+    if (com_d && nc > 0)
+        cudaMemcpyAsync(com_d, w->b.com, 16 * (size_t)nc, cudaMemcpyDeviceToDevice, st);
+    if (cudaStreamSynchronize(st) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+        return ORRERY_ECUDA;
+    return nn > max_nodes ? ORRERY_ERANGE : ORRERY_OK;
+}
+
+int64_t orrery_bh_max_nodes(int64_t n, int32_t leaf_cap)
+{
+    if (n < 0 || n > kMaxN || leaf_cap < 1) return -1;
+    return node_bound(n, leaf_cap);
+}
+
+int orrery_bh_last_timings(orrery_bh_timings *out)
+{
+    if (!out) return ORRERY_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_have_last) return ORRERY_EINVAL;
+    *out = g_last;
+    return ORRERY_OK;
+}
+
+uint64_t orrery_bh_kernel_launches(void) { return g_launches.load(); }
+
+const char *orrery_bh_strerror(int status)
+{
+    switch (status) {
+    case ORRERY_OK: return "ok";
+    case ORRERY_EINVAL: return "invalid argument";
+    case ORRERY_ENONFINITE: return "non-finite position or mass";
+    case ORRERY_ERANGE: return "node count or size beyond the int32 range";
+    case ORRERY_ECUDA: return "CUDA runtime error";
+    case ORRERY_EWALK: return "walk exceeded its iteration bound";
+    case ORRERY_ENOMEM: return "workspace allocation failed";
+    case ORRERY_EINTERNAL: return "internal consistency check failed";
+    default: return "unknown status";
+    }
+}
+
+void orrery_bh_release(void)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int d = 0; d < kMaxDevices; ++d) {
+        free_workspace(g_ws[d]);
+        g_ws[d] = nullptr;
+    }
+    g_have_last = false;
+}
+
+}  // extern "C"

@@ -1,0 +1,230 @@
+// bh_build.cu -- a5 octree build from sorted Morton keys and a6 upward
+// monopole moments.
+//
+// Tree definition (orrery: "sycl_tree_solver.hpp", "Where the tree comes
+// from"; ADR-0029, Decision; the workload's "split any cell above leaf
+// capacity"): a cell of level L is the run of sorted keys sharing their top L
+// octant digits. The root is a node; any other cell is a node iff its parent
+// cell holds more than leaf_cap particles (and so do all its ancestors,
+// since counts only grow upwards). A node is a leaf iff it holds at most
+// leaf_cap particles or its level is 21. Nodes are stored in depth-first
+// preorder with the escape index of each node = first node after its subtree.
+//
+// The build is flat rather than recursive. Two observations make it so:
+//  * in preorder, nodes are ordered by (first particle, level), so the index
+//    of a node is (nodes starting at earlier positions) + (its rank among
+//    the nested nodes that start at the same position): one exclusive scan of
+//    a per-position node count;
+//  * the nodes starting at position i are the cells of levels D+1 .. L_last,
+//    where D is the number of levels key[i-1] and key[i] share, provided the
+//    level-D cell around them is over capacity; the chain stops at the first
+//    level whose cell does not contain key[i + leaf_cap] (or at level 21).
+// escape(node) = scan value at the first position past the node's range.
+#include "bh_common.cuh"
+
+namespace obh {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Per position: D (levels shared with the previous key), W (levels shared
+// with the key leaf_cap ahead), the number of nodes starting here, and the
+// start of the parent cell of the first of them.
+__global__ void __launch_bounds__(kThreads)
+k_build_levels(const uint64_t *__restrict__ K, int64_t n, int32_t cap,
+               int8_t *__restrict__ lev_d, int8_t *__restrict__ lev_w,
+               uint8_t *__restrict__ ncount, int32_t *__restrict__ pstart)
+{
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i > n) return;
+    if (i == n) {  // the scan runs over n + 1 entries; the last contributes 0
+        ncount[n] = 0;
+        return;
+    }
+    const uint64_t key = K[i];
+    const int D = (i == 0) ? -1 : common_levels(K[i - 1], key);
+    const int W = (i + cap < n) ? common_levels(key, K[i + cap]) : -1;
+    int cnt = 0;
+    int64_t s = 0;
+    if (i == 0) {
+        cnt = (W < 0) ? 1 : min(kLevels, W + 1) + 1;  // levels 0 .. L_last
+    } else if (D < kLevels) {
+        // start of the level-D cell holding key[i-1] and key[i]: the first
+        // position whose key is >= key with its low 3(21-D) bits cleared
+        const uint64_t prefix = key & ~((1ull << (3 * (kLevels - D))) - 1ull);
+        int64_t lo = 0, hi = i;
+        while (lo < hi) {
+            int64_t mid = (lo + hi) >> 1;
+            if (K[mid] < prefix)
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        s = lo;
+        const int Ws = (s + cap < n) ? common_levels(K[s], K[s + cap]) : -1;
+        if (Ws >= D) cnt = min(kLevels, max(D + 1, W + 1)) - D;  // parent over capacity
+    }
+    lev_d[i] = (int8_t)D;
+    lev_w[i] = (int8_t)W;
+    ncount[i] = (uint8_t)cnt;
+    pstart[i] = (int32_t)s;
+}
+
+// Writes the nodes that start at each position: {escape, first, count, level},
+// the parent index, and counts children with an atomic add on the parent.
+__global__ void __launch_bounds__(kThreads)
+k_build_emit(const uint64_t *__restrict__ K, int64_t n, const int8_t *__restrict__ lev_d,
+             const uint8_t *__restrict__ ncount, const int32_t *__restrict__ pstart,
+             const uint32_t *__restrict__ node_start, int64_t max_nodes, int4 *__restrict__ meta,
+             int32_t *__restrict__ parent, int32_t *__restrict__ nchild, DeviceParams *P)
+{
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const uint32_t total = node_start[n];
+    if (i == 0) {
+        P->num_nodes = (int)total;
+        if ((int64_t)total > max_nodes) atomicOr(&P->status, kStatusNodeBound);
+    }
+    const int cnt = ncount[i];
+    if (cnt == 0 || (int64_t)total > max_nodes) return;
+    const uint64_t key = K[i];
+    const int D = lev_d[i];
+    const int first_level = (i == 0) ? 0 : D + 1;
+    const uint32_t base = node_start[i];
+    int32_t par = -1;
+    if (i > 0) {
+        const int64_t s = pstart[i];
+        const int s_first_level = (s == 0) ? 0 : lev_d[s] + 1;
+        par = (int32_t)(node_start[s] + (uint32_t)(D - s_first_level));
+        if (par < 0 || par >= (int32_t)base) {  // a parent precedes its children
+            atomicOr(&P->status, kStatusInternal);
+            return;
+        }
+    }
+    int64_t hi = n;  // the cells starting at i are nested: each ends no later
+    for (int j = 0; j < cnt; ++j) {
+        const int L = first_level + j;
+        const int64_t k = (int64_t)base + j;
+        int64_t end = n;
+        if (L > 0) {
+            const uint64_t upper = key | ((1ull << (3 * (kLevels - L))) - 1ull);
+            int64_t lo = i + 1, h = hi;
+            while (lo < h) {
+                int64_t mid = (lo + h) >> 1;
+                if (K[mid] <= upper)
+                    lo = mid + 1;
+                else
+                    h = mid;
+            }
+            end = lo;
+        }
+        hi = end;
+        meta[k] = make_int4((int)node_start[end], (int)i, (int)(end - i), L);
+        parent[k] = par;
+        if (par >= 0) atomicAdd(&nchild[par], 1);
+        par = (int32_t)k;
+    }
+    atomicMax(&P->depth, first_level + cnt - 1);
+}
+
+__device__ __forceinline__ void store_moments(int64_t k, float sx, float sy, float sz, float M,
+                                              float4 *sums, float4 *com)
+{
+    __stcg(sums + k, make_float4(sx, sy, sz, M));
+    float4 c = make_float4(0.0f, 0.0f, 0.0f, M);
+    if (M > 0.0f) {
+        c.x = __fdiv_rn(sx, M);
+        c.y = __fdiv_rn(sy, M);
+        c.z = __fdiv_rn(sz, M);
+    }
+    __stcg(com + k, c);
+}
+
+// a6: one thread per leaf (the last node of each position's chain) sums its
+// particles in sorted order, then climbs: the last child to arrive at a
+// parent (atomic arrival count == child count) sums all of the parent's
+// children in child order. No thread ever waits for another.
+__global__ void __launch_bounds__(kThreads)
+k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ ncount,
+          const uint32_t *__restrict__ node_start, const int4 *__restrict__ meta,
+          const int32_t *__restrict__ parent, const int32_t *__restrict__ nchild,
+          int32_t *__restrict__ arrive, float4 *sums, float4 *com, DeviceParams *P)
+{
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int cnt = ncount[i];
+    if (cnt == 0 || (P->status & kStatusNodeBound)) return;
+    int64_t k = (int64_t)node_start[i] + cnt - 1;
+    const int4 m = meta[k];
+    if (m.y < 0 || m.z < 0 || (int64_t)m.y + m.z > n) {
+        atomicOr((int *)&P->status, kStatusInternal);
+        return;
+    }
+    const int total = P->num_nodes;
+    float M = 0.0f, sx = 0.0f, sy = 0.0f, sz = 0.0f;
+    for (int64_t j = m.y; j < (int64_t)m.y + m.z; ++j) {
+        const float4 p = __ldg(ps + j);
+        M = __fadd_rn(M, p.w);
+        sx = __fmaf_rn(p.w, p.x, sx);
+        sy = __fmaf_rn(p.w, p.y, sy);
+        sz = __fmaf_rn(p.w, p.z, sz);
+    }
+    store_moments(k, sx, sy, sz, M, sums, com);
+    int64_t node = parent[k];
+    while (node >= 0) {
+        __threadfence();
+        const int prev = atomicAdd(arrive + node, 1);
+        if (prev != nchild[node] - 1) return;
+        __threadfence();
+        const int esc = meta[node].x;
+        M = sx = sy = sz = 0.0f;
+        if (esc > total) {
+            atomicOr((int *)&P->status, kStatusInternal);
+            return;
+        }
+        for (int c = (int)node + 1; c < esc;) {
+            const float4 s = __ldcg(sums + c);
+            M = __fadd_rn(M, s.w);
+            sx = __fadd_rn(sx, s.x);
+            sy = __fadd_rn(sy, s.y);
+            sz = __fadd_rn(sz, s.z);
+            const int nc = meta[c].x;
+            if (nc <= c) {  // escapes strictly increase; stop rather than loop
+                atomicOr((int *)&P->status, kStatusInternal);
+                return;
+            }
+            c = nc;
+        }
+        store_moments(node, sx, sy, sz, M, sums, com);
+        node = parent[node];
+    }
+}
+
+}  // namespace
+
+void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b,
+                  cudaStream_t st)
+{
+    k_build_levels<<<ceil_div(b.n + 1, kThreads), kThreads, 0, st>>>(
+        keys_sorted, b.n, leaf_cap, b.lev_d, b.lev_w, b.ncount, b.pstart);
+    g_launches += 1;
+    // node_start = exclusive scan of ncount over n + 1 entries
+    launch_scan_u8(b.ncount, b.node_start, b.n + 1, b.scan_partial, st);
+    cudaMemsetAsync(b.nchild, 0, sizeof(int32_t) * (size_t)b.max_nodes, st);
+    k_build_emit<<<ceil_div(b.n, kThreads), kThreads, 0, st>>>(
+        keys_sorted, b.n, b.lev_d, b.ncount, b.pstart, b.node_start, b.max_nodes, b.meta,
+        b.parent, b.nchild, b.params);
+    g_launches += 1;
+}
+
+void launch_moments(int32_t leaf_cap, const Buffers &b, cudaStream_t st)
+{
+    (void)leaf_cap;
+    cudaMemsetAsync(b.arrive, 0, sizeof(int32_t) * (size_t)b.max_nodes, st);
+    k_moments<<<ceil_div(b.n, kThreads), kThreads, 0, st>>>(b.ps, b.n, b.ncount, b.node_start,
+                                                           b.meta, b.parent, b.nchild, b.arrive,
+                                                           b.sums, b.com, b.params);
+    g_launches += 1;
+}
+
+}  // namespace obh

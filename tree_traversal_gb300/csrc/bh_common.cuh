@@ -1,0 +1,106 @@
+// bh_common.cuh -- types and helpers shared by the CUDA translation units of
+// the Barnes-Hut library (never by the oracle).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+namespace obh {
+
+constexpr int kLevels = 21;          // bits per axis; deepest octree level
+constexpr int kWarp = 32;
+
+// Bits of the device status word.
+constexpr int kStatusNonFinite = 1;  // a position or mass is not finite
+constexpr int kStatusWalkBound = 2;  // a walk hit its iteration bound
+constexpr int kStatusNodeBound = 4;  // more nodes than the workspace holds
+constexpr int kStatusInternal = 8;   // an index failed a consistency check (access skipped)
+
+// Per-evaluation parameters that the device computes for itself.
+struct DeviceParams {
+    float lo[3];
+    float side;
+    float inv;
+    float s2[kLevels + 1];  // (side * 2^-L)^2 for L = 0..21
+    int status;
+    int num_nodes;
+    int depth;
+    int pad;
+};
+
+// Device pointers carved out of one workspace allocation.
+struct Buffers {
+    int64_t n;
+    int64_t max_nodes;
+    int radix_blocks;
+    int bbox_blocks;
+    // a1
+    float *bbox_partial;      // [bbox_blocks][8]
+    DeviceParams *params;
+    // a2, a3
+    uint64_t *keys_a, *keys_b;
+    uint32_t *idx_a, *idx_b;
+    uint32_t *radix_hist;     // [256][radix_blocks], digit-major
+    uint32_t *radix_total;    // [256]
+    // a4
+    float4 *ps;               // sorted {x, y, z, m}
+    // a5
+    int8_t *lev_d;            // common levels with the previous key (-1 at 0)
+    int8_t *lev_w;            // common levels with the key leaf_cap ahead (-1 if none)
+    uint8_t *ncount;          // nodes starting at each position
+    int32_t *pstart;          // start of the parent cell of the first node at i
+    uint32_t *node_start;     // [n + 1] exclusive scan of ncount
+    uint32_t *scan_partial;   // scan block sums
+    int4 *meta;               // [max_nodes] {escape, first, count, level}
+    int32_t *parent;          // [max_nodes]
+    int32_t *nchild;          // [max_nodes]
+    int32_t *arrive;          // [max_nodes]
+    // a6
+    float4 *sums;             // [max_nodes] {S_x, S_y, S_z, M}
+    float4 *com;              // [max_nodes] {CoM_x, CoM_y, CoM_z, M}
+    // a7
+    float *acc_s;             // [n][3] sorted order
+    uint32_t *cnt_s;          // [n][3] {pc, pp, visits} sorted order
+};
+
+// Kernel-launch counter (every launch site increments it).
+extern std::atomic<uint64_t> g_launches;
+
+// --- launchers, one per phase (all enqueue on `st`) ----------------------
+void launch_bbox(const float *pos, const float *mass, const Buffers &b, cudaStream_t st);
+void launch_morton(const float *pos, const Buffers &b, cudaStream_t st);
+void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint32_t **perm);
+void launch_gather(const float *pos, const float *mass, const uint32_t *perm, const Buffers &b,
+                   cudaStream_t st);
+void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b,
+                  cudaStream_t st);
+void launch_moments(int32_t leaf_cap, const Buffers &b, cudaStream_t st);
+void launch_walk(int traversal, float theta, float eps, int32_t leaf_cap, bool count,
+                 const Buffers &b, cudaStream_t st);
+void launch_scatter(const uint32_t *perm, const Buffers &b, float *acc, uint32_t *inter,
+                    uint32_t *visits, cudaStream_t st);
+void launch_scan_u32(const uint32_t *in, uint32_t *out, int64_t count, uint32_t *partial,
+                     cudaStream_t st);
+void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *partial,
+                    cudaStream_t st);
+int64_t scan_partial_count(int64_t count);
+int radix_blocks_for(int64_t n);
+
+// --- small device helpers -------------------------------------------------
+// Number of leading 3-bit groups (levels) two 63-bit keys share: 0..21.
+__device__ __forceinline__ int common_levels(uint64_t a, uint64_t b)
+{
+    uint64_t x = a ^ b;
+    if (x == 0) return kLevels;
+    int msb = 63 - __clzll((long long)x);
+    return (kLevels - 1) - msb / 3;
+}
+
+__device__ __forceinline__ float4 ldg_f4(const float4 *p) { return __ldg(p); }
+__device__ __forceinline__ int4 ldg_i4(const int4 *p) { return __ldg(p); }
+
+inline unsigned ceil_div(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b); }
+
+}  // namespace obh

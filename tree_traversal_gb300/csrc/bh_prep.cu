@@ -1,0 +1,327 @@
+// bh_prep.cu -- the data-movement phases around the tree: bounding cube,
+// Morton keys, gather into tree order, scatter back, and a device-wide
+// exclusive scan used by the build.
+//
+// Pages: "sycl_tree_solver.hpp" (Detailed Description, "Where the tree comes
+// from": particles are copied into the tree's sorted order before the walk
+// and the accelerations scattered back to the caller's order afterwards).
+// The bounding cube and the 21-bit key follow the workload definition that
+// accompanies the pages (a quantised bounding cube, 21 bits per axis).
+#include <math.h>
+
+#include "bh_common.cuh"
+
+namespace obh {
+
+std::atomic<uint64_t> g_launches{0};
+
+namespace {
+
+constexpr int kBBoxThreads = 256;
+
+__device__ __forceinline__ void warp_minmax(float &lo, float &hi)
+{
+    for (int off = 16; off > 0; off >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+    }
+}
+
+// a1, part 1: per-block min / max per axis and a non-finite flag.
+__global__ void __launch_bounds__(kBBoxThreads)
+k_bbox_partial(const float *__restrict__ pos, const float *__restrict__ mass, int64_t n,
+               float *__restrict__ partial)
+{
+    float lo[3] = {INFINITY, INFINITY, INFINITY};
+    float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
+    int bad = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float m = __ldg(mass + i);
+        bad |= !isfinite(m);
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+            float x = __ldg(pos + 3 * i + a);
+            bad |= !isfinite(x);
+            lo[a] = fminf(lo[a], x);
+            hi[a] = fmaxf(hi[a], x);
+        }
+    }
+    __shared__ float s_lo[3][kBBoxThreads / 32], s_hi[3][kBBoxThreads / 32];
+    __shared__ int s_bad[kBBoxThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) warp_minmax(lo[a], hi[a]);
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+        for (int a = 0; a < 3; ++a) {
+            s_lo[a][warp] = lo[a];
+            s_hi[a][warp] = hi[a];
+        }
+        s_bad[warp] = bad;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kBBoxThreads / 32; ++w) {
+            for (int a = 0; a < 3; ++a) {
+                lo[a] = fminf(lo[a], s_lo[a][w]);
+                hi[a] = fmaxf(hi[a], s_hi[a][w]);
+            }
+            bad |= s_bad[w];
+        }
+        float *o = partial + 8 * blockIdx.x;
+        for (int a = 0; a < 3; ++a) {
+            o[a] = lo[a];
+            o[3 + a] = hi[a];
+        }
+        o[6] = bad ? 1.0f : 0.0f;
+    }
+}
+
+// a1, part 2: one block folds the partials and derives the cube:
+// side = max_a (hi_a - lo_a), inv = 2^21 / side, and the per-level squared
+// cell side s2[L] = (side * side) * 2^(-2L) (an exact power-of-two scaling).
+// Also resets the status word, node count and depth of this evaluation.
+__global__ void k_bbox_final(const float *__restrict__ partial, int blocks, DeviceParams *P)
+{
+    if (threadIdx.x != 0) return;
+    float lo[3] = {INFINITY, INFINITY, INFINITY};
+    float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
+    int bad = 0;
+    for (int b = 0; b < blocks; ++b) {
+        const float *o = partial + 8 * b;
+        for (int a = 0; a < 3; ++a) {
+            lo[a] = fminf(lo[a], o[a]);
+            hi[a] = fmaxf(hi[a], o[3 + a]);
+        }
+        bad |= (o[6] != 0.0f);
+    }
+    float side = 0.0f;
+    for (int a = 0; a < 3; ++a) {
+        float ext = __fsub_rn(hi[a], lo[a]);
+        if (ext > side) side = ext;
+        P->lo[a] = lo[a];
+    }
+    P->side = side;
+    P->inv = (side > 0.0f) ? __fdiv_rn(2097152.0f, side) : 0.0f;
+    float s2 = __fmul_rn(side, side);
+    for (int L = 0; L <= kLevels; ++L) P->s2[L] = __fmul_rn(s2, ldexpf(1.0f, -2 * L));
+    P->status = bad ? kStatusNonFinite : 0;
+    P->num_nodes = 0;
+    P->depth = 0;
+}
+
+// Spreads the low 21 bits of v so that bit b lands at bit 3b.
+__device__ __forceinline__ uint64_t spread3(uint32_t v)
+{
+    uint64_t x = v & 0x1fffffu;
+    x = (x | (x << 32)) & 0x001f00000000ffffull;
+    x = (x | (x << 16)) & 0x001f0000ff0000ffull;
+    x = (x | (x << 8)) & 0x100f00f00f00f00full;
+    x = (x | (x << 4)) & 0x10c30c30c30c30c3ull;
+    x = (x | (x << 2)) & 0x1249249249249249ull;
+    return x;
+}
+
+// q = min(floor(fl(fl(x - lo) * inv)), 2^21 - 1)
+__device__ __forceinline__ uint32_t quantise(float x, float lo, float inv)
+{
+    float t = __fmul_rn(__fsub_rn(x, lo), inv);
+    if (!(t >= 0.0f)) t = 0.0f;
+    if (t >= 2097151.0f) return 2097151u;
+    return (uint32_t)t;  // truncation is floor for t >= 0
+}
+
+// a2: 63-bit Morton key per particle, x the high bit of each level's triple.
+__global__ void __launch_bounds__(256)
+k_morton(const float *__restrict__ pos, int64_t n, const DeviceParams *__restrict__ P,
+         uint64_t *__restrict__ keys)
+{
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float inv = P->inv;
+    uint32_t qx = quantise(__ldg(pos + 3 * i + 0), P->lo[0], inv);
+    uint32_t qy = quantise(__ldg(pos + 3 * i + 1), P->lo[1], inv);
+    uint32_t qz = quantise(__ldg(pos + 3 * i + 2), P->lo[2], inv);
+    keys[i] = (spread3(qx) << 2) | (spread3(qy) << 1) | spread3(qz);
+}
+
+// a4: sorted particles {x, y, z, m}.
+__global__ void __launch_bounds__(256)
+k_gather(const float *__restrict__ pos, const float *__restrict__ mass,
+         const uint32_t *__restrict__ perm, int64_t n, float4 *__restrict__ ps, int *status)
+{
+    int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= n) return;
+    uint32_t i = __ldg(perm + k);
+    if (i >= (uint64_t)n) {
+        atomicOr(status, kStatusInternal);
+        return;
+    }
+    ps[k] = make_float4(__ldg(pos + 3 * (int64_t)i), __ldg(pos + 3 * (int64_t)i + 1),
+                        __ldg(pos + 3 * (int64_t)i + 2), __ldg(mass + i));
+}
+
+// a8: results back to the caller's order.
+__global__ void __launch_bounds__(256)
+k_scatter(const uint32_t *__restrict__ perm, int64_t n, const float *__restrict__ acc_s,
+          const uint32_t *__restrict__ cnt_s, float *__restrict__ acc,
+          uint32_t *__restrict__ inter, uint32_t *__restrict__ visits, int *status)
+{
+    int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= n) return;
+    int64_t i = __ldg(perm + k);
+    if (i >= n) {
+        atomicOr(status, kStatusInternal);
+        return;
+    }
+    acc[3 * i + 0] = acc_s[3 * k + 0];
+    acc[3 * i + 1] = acc_s[3 * k + 1];
+    acc[3 * i + 2] = acc_s[3 * k + 2];
+    if (inter) {
+        inter[2 * i + 0] = cnt_s[3 * k + 0];
+        inter[2 * i + 1] = cnt_s[3 * k + 1];
+    }
+    if (visits) visits[i] = cnt_s[3 * k + 2];
+}
+
+// ---- exclusive scan of uint32 (three launches, no inter-block waiting) ----
+constexpr int kScanThreads = 256;
+constexpr int kScanItems = 8;
+constexpr int kScanTile = kScanThreads * kScanItems;
+
+// Block-wide exclusive scan of one value per thread; returns the block total.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t &total)
+{
+    __shared__ uint32_t s_warp[kScanThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = (lane < kScanThreads / 32) ? s_warp[lane] : 0u;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            uint32_t y = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += y;
+        }
+        if (lane < kScanThreads / 32) s_warp[lane] = w;
+    }
+    __syncthreads();
+    uint32_t before = (warp > 0) ? s_warp[warp - 1] : 0u;
+    total = s_warp[kScanThreads / 32 - 1];
+    __syncthreads();
+    return before + x - v;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kScanThreads)
+k_scan_reduce(const T *__restrict__ in, int64_t count, uint32_t *__restrict__ partial)
+{
+    int64_t base = (int64_t)blockIdx.x * kScanTile + threadIdx.x * kScanItems;
+    uint32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j)
+        if (base + j < count) s += in[base + j];
+    uint32_t total;
+    block_exclusive_scan(s, total);
+    if (threadIdx.x == 0) partial[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+k_scan_partials(uint32_t *__restrict__ partial, int64_t parts)
+{
+    uint32_t carry = 0;
+    for (int64_t base = 0; base < parts; base += kScanThreads) {
+        int64_t i = base + threadIdx.x;
+        uint32_t v = (i < parts) ? partial[i] : 0u;
+        uint32_t total;
+        uint32_t ex = block_exclusive_scan(v, total);
+        if (i < parts) partial[i] = carry + ex;
+        carry += total;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kScanThreads)
+k_scan_down(const T *__restrict__ in, uint32_t *__restrict__ out, int64_t count,
+            const uint32_t *__restrict__ partial)
+{
+    int64_t base = (int64_t)blockIdx.x * kScanTile + threadIdx.x * kScanItems;
+    uint32_t v[kScanItems];
+    uint32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j) {
+        v[j] = (base + j < count) ? in[base + j] : 0u;
+        s += v[j];
+    }
+    uint32_t total;
+    uint32_t run = block_exclusive_scan(s, total) + partial[blockIdx.x];
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j) {
+        if (base + j < count) out[base + j] = run;
+        run += v[j];
+    }
+}
+
+}  // namespace
+
+int64_t scan_partial_count(int64_t count) { return (count + kScanTile - 1) / kScanTile; }
+
+template <typename T>
+static void scan_exclusive(const T *in, uint32_t *out, int64_t count, uint32_t *partial,
+                           cudaStream_t st)
+{
+    int64_t parts = scan_partial_count(count);
+    k_scan_reduce<T><<<(unsigned)parts, kScanThreads, 0, st>>>(in, count, partial);
+    k_scan_partials<<<1, kScanThreads, 0, st>>>(partial, parts);
+    k_scan_down<T><<<(unsigned)parts, kScanThreads, 0, st>>>(in, out, count, partial);
+    g_launches += 3;
+}
+
+void launch_scan_u32(const uint32_t *in, uint32_t *out, int64_t count, uint32_t *partial,
+                     cudaStream_t st)
+{
+    scan_exclusive<uint32_t>(in, out, count, partial, st);
+}
+
+void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *partial,
+                    cudaStream_t st)
+{
+    scan_exclusive<uint8_t>(in, out, count, partial, st);
+}
+
+void launch_bbox(const float *pos, const float *mass, const Buffers &b, cudaStream_t st)
+{
+    k_bbox_partial<<<b.bbox_blocks, kBBoxThreads, 0, st>>>(pos, mass, b.n, b.bbox_partial);
+    k_bbox_final<<<1, 32, 0, st>>>(b.bbox_partial, b.bbox_blocks, b.params);
+    g_launches += 2;
+}
+
+void launch_morton(const float *pos, const Buffers &b, cudaStream_t st)
+{
+    k_morton<<<ceil_div(b.n, 256), 256, 0, st>>>(pos, b.n, b.params, b.keys_a);
+    g_launches += 1;
+}
+
+void launch_gather(const float *pos, const float *mass, const uint32_t *perm, const Buffers &b,
+                   cudaStream_t st)
+{
+    k_gather<<<ceil_div(b.n, 256), 256, 0, st>>>(pos, mass, perm, b.n, b.ps, &b.params->status);
+    g_launches += 1;
+}
+
+void launch_scatter(const uint32_t *perm, const Buffers &b, float *acc, uint32_t *inter,
+                    uint32_t *visits, cudaStream_t st)
+{
+    k_scatter<<<ceil_div(b.n, 256), 256, 0, st>>>(perm, b.n, b.acc_s, b.cnt_s, acc, inter, visits,
+                                                   &b.params->status);
+    g_launches += 1;
+}
+
+}  // namespace obh
