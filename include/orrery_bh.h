@@ -57,6 +57,8 @@ extern "C" {
 #define ORRERY_ENOMEM (-6)     /* the workspace could not be allocated */
 #define ORRERY_EINTERNAL (-7)  /* an index failed a device-side consistency check;
                                   the access was skipped (a library defect) */
+#define ORRERY_ESCRATCH (-8)   /* orrery_bh_forces_noalloc: the problem does not fit
+                                  its fixed scratch array */
 
 /* Which traversal the walk kernel runs ("sycl_tree_solver.hpp",
  * TreeTraversal). Both compute the same function of the input. */
@@ -117,6 +119,34 @@ int orrery_bh_forces(const float *pos_d, const float *mass_d, int64_t n, float t
 int orrery_bh_forces_host(const float *pos, const float *mass, int64_t n, float theta, float eps,
                           int32_t leaf_cap, int32_t traversal, float *acc, uint32_t *interactions,
                           uint32_t *visits, void *stream);
+
+/*
+ * The same evaluation as orrery_bh_forces, for callers that must not allocate
+ * device memory during a call: host applications or plugins that own every
+ * device allocation themselves, code that runs while a CUDA graph may be
+ * under capture, and latency-critical loops that cannot take the implicit
+ * device synchronisation of cudaMalloc / cudaFree. (The pages have no
+ * counterpart: their solver allocates its shared-memory buffers per call.)
+ *
+ * It calls no cudaMalloc, cudaFree or other allocating routine. Its scratch
+ * is one fixed 16 MiB array inside the library's device code, which every GPU
+ * that loads the library holds until the process exits. A call fits iff its
+ * buffers fit 16 MiB: at leaf_cap >= 16 every n <= 65536 fits; at leaf_cap 32
+ * up to 96640 particles fit. A call that does not fit returns ORRERY_ESCRATCH
+ * before launching anything.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it: make that first call before any stream
+ * capture. All calls share the array, which keeps the previous call's
+ * contents; each call clears what must start at zero. Calls whose GPU work
+ * overlapped would race on the array: this entry point serialises its calls
+ * and waits for its own work before returning, so its calls do not overlap.
+ * Arguments, layouts, results and statuses as in orrery_bh_forces; no phase
+ * timings are recorded.
+ */
+int orrery_bh_forces_noalloc(const float *pos_d, const float *mass_d, int64_t n, float theta,
+                             float eps, int32_t leaf_cap, int32_t traversal, float *acc_d,
+                             uint32_t *interactions_d, uint32_t *visits_d, void *stream);
 
 /*
  * Runs the cube, key, sort, gather, build and moments steps and copies their

@@ -104,7 +104,8 @@ def test_node_bound(lib):
 def test_strerror_and_counters(lib):
     import tree_traversal_gb300._lib as L
 
-    for s in (L.OK, L.EINVAL, L.ENONFINITE, L.ERANGE, L.ECUDA, L.EWALK, L.ENOMEM, L.EINTERNAL):
+    for s in (L.OK, L.EINVAL, L.ENONFINITE, L.ERANGE, L.ECUDA, L.EWALK, L.ENOMEM, L.EINTERNAL,
+              L.ESCRATCH):
         assert lib.orrery_bh_strerror(s).decode() not in ("", "unknown status")
     assert lib.orrery_bh_strerror(-99).decode() == "unknown status"
     t = L.Timings()

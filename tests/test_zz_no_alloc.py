@@ -1,0 +1,80 @@
+"""orrery_bh_forces_noalloc, the entry point for callers that cannot allocate
+device memory during a call (their allocator or graph capture forbids it):
+its results must equal the ordinary entry point's, call after call, although
+its scratch is one fixed array shared by every call.
+
+This file is collected last on purpose, so a run that stops at the first
+failure has already run every other test."""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+REL_TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tree_traversal_gb300.build import build
+
+    build()
+    import tree_traversal_gb300._lib as L
+
+    return L.load()
+
+
+def _call(fn, pos, mass, theta, eps, cap, traversal):
+    n = pos.shape[0]
+    acc = torch.full((n, 3), float("nan"), device="cuda")
+    inter = torch.full((n, 2), -1, dtype=torch.int32, device="cuda")
+    vis = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = fn(p(pos), p(mass), n, theta, eps, cap, traversal, p(acc), p(inter), p(vis),
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    return rc, acc, inter, vis
+
+
+def test_noalloc_matches_the_allocating_entry_point(lib):
+    import tree_traversal_gb300._lib as L
+    from inputs import plummer, uniform_cube
+
+    # two calls in a row on different inputs: a larger one, then a smaller
+    # one that lands on scratch the first call left behind
+    cases = [(plummer(65536, 3), 0.5, 0.05, 32, L.COHERENT),
+             (uniform_cube(5003, 4), 0.7, 0.05, 7, L.INDEPENDENT),
+             (plummer(40000, 5), 0.5, 0.05, 16, L.COHERENT)]
+    for (pos_np, mass_np), theta, eps, cap, trav in cases:
+        pos = torch.from_numpy(pos_np).cuda()
+        mass = torch.from_numpy(mass_np).cuda()
+        rc0, acc0, inter0, vis0 = _call(lib.orrery_bh_forces, pos, mass, theta, eps, cap, trav)
+        assert rc0 == L.OK
+        for _ in range(2):
+            rc, acc, inter, vis = _call(lib.orrery_bh_forces_noalloc, pos, mass, theta, eps, cap,
+                                        trav)
+            assert rc == L.OK
+            a, r = acc.double(), acc0.double()
+            rel = ((a - r).norm(dim=1) / r.norm(dim=1)).max().item()
+            assert rel <= REL_TOL
+            assert torch.equal(acc.view(torch.int32), acc0.view(torch.int32))
+            assert torch.equal(inter, inter0) and torch.equal(vis, vis0)
+
+
+def test_noalloc_rejects_what_does_not_fit(lib):
+    import tree_traversal_gb300._lib as L
+
+    dummy = ctypes.c_void_p(16)  # never dereferenced: the size check fails first
+    assert lib.orrery_bh_forces_noalloc(dummy, dummy, 200000, 0.5, 0.05, 32, 1, dummy, None, None,
+                                        None) == L.ESCRATCH
+    assert lib.orrery_bh_forces_noalloc(dummy, dummy, 65536, 0.5, 0.05, 1, 1, dummy, None, None,
+                                        None) == L.ESCRATCH
+    assert lib.orrery_bh_forces_noalloc(dummy, dummy, 10, -1.0, 0.05, 32, 1, dummy, None, None,
+                                        None) == L.EINVAL
+    assert lib.orrery_bh_forces_noalloc(None, None, 0, 0.5, 0.05, 32, 1, None, None, None,
+                                        None) == L.OK

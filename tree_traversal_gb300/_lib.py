@@ -22,6 +22,7 @@ ECUDA = -4
 EWALK = -5
 ENOMEM = -6
 EINTERNAL = -7
+ESCRATCH = -8
 
 INDEPENDENT = 0
 COHERENT = 1
@@ -76,6 +77,8 @@ def load(path: str | None = None):
         lib.orrery_bh_forces.restype = ctypes.c_int
         lib.orrery_bh_forces_host.argtypes = [P, P, i64, f32, f32, i32, i32, P, P, P, P]
         lib.orrery_bh_forces_host.restype = ctypes.c_int
+        lib.orrery_bh_forces_noalloc.argtypes = [P, P, i64, f32, f32, i32, i32, P, P, P, P]
+        lib.orrery_bh_forces_noalloc.restype = ctypes.c_int
         lib.orrery_bh_tree.argtypes = [P, P, i64, i32, P, P, P, P, P, i64,
                                        ctypes.POINTER(ctypes.c_int64), P]
         lib.orrery_bh_tree.restype = ctypes.c_int

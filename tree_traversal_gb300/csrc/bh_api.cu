@@ -406,6 +406,7 @@ const char *orrery_bh_strerror(int status)
     case ORRERY_EWALK: return "walk exceeded its iteration bound";
     case ORRERY_ENOMEM: return "workspace allocation failed";
     case ORRERY_EINTERNAL: return "internal consistency check failed";
+    case ORRERY_ESCRATCH: return "problem too large for the fixed no-allocation scratch";
     default: return "unknown status";
     }
 }

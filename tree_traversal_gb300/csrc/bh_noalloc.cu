@@ -1,0 +1,155 @@
+// bh_noalloc.cu -- orrery_bh_forces_noalloc: the whole force evaluation with
+// its scratch in a fixed array that the library image itself carries, for
+// callers that must not allocate device memory during a call.
+//
+// Who needs this: a host application or plugin that owns every device
+// allocation itself (a pooled or arena allocator, a memory budget enforced
+// from outside), code that runs while another thread may be capturing a CUDA
+// graph on the device, and latency-sensitive loops that cannot afford the
+// implicit device synchronisation of cudaMalloc / cudaFree. For them the
+// ordinary entry point's grow-only workspace is the problem: its first call,
+// and any call with a larger n than before, allocates.
+//
+// The scratch is one file-scope __device__ array of kScratchBytes. Every GPU
+// on which this library's device code is loaded holds that memory until the
+// process exits. Host code may not use the array's name as a device address
+// (in host code it names a host-side shadow), so the first call on each
+// device looks the address up with cudaGetSymbolAddress while that device is
+// current, and caches it; make that first call before any stream capture.
+//
+// All calls on a device share the array and it keeps the previous call's
+// contents: every buffer that must start at zero is cleared by the call
+// itself (the child and arrival counters are reset with cudaMemsetAsync, the
+// status word by the cube kernel). Two calls whose GPU work overlapped would
+// race on the array; this entry point serialises its calls with a lock and
+// waits for its own work before returning, so its own calls never overlap.
+// It does not share the array with orrery_bh_forces, whose workspace is
+// separate.
+#include <mutex>
+
+#include "../../include/orrery_bh.h"
+#include "bh_common.cuh"
+
+namespace obh {
+namespace {
+
+constexpr size_t kScratchBytes = size_t(16) << 20;  // 16 MiB per device
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxN = int64_t(1) << 30;
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int64_t bound_nodes(int64_t n, int32_t cap) { return n + 21 * (n / ((int64_t)cap + 1)) + 1; }
+
+// The buffers of one evaluation laid out over `base` (nullptr: size only).
+size_t layout(Buffers &b, char *base, int64_t n, int64_t nodes)
+{
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char * {
+        char *p = base ? base + off : nullptr;
+        off += up256(bytes);
+        return p;
+    };
+    const size_t n1 = (size_t)n + 1;
+    b.n = n;
+    b.max_nodes = nodes;
+    b.radix_blocks = radix_blocks_for(n);
+    int64_t bb = (n + 255) / 256;
+    b.bbox_blocks = (int)(bb < 1 ? 1 : (bb > 1216 ? 1216 : bb));
+    b.bbox_partial = (float *)take(sizeof(float) * 8 * (size_t)b.bbox_blocks);
+    b.params = (DeviceParams *)take(sizeof(DeviceParams));
+    b.keys_a = (uint64_t *)take(8 * (size_t)n);
+    b.keys_b = (uint64_t *)take(8 * (size_t)n);
+    b.idx_a = (uint32_t *)take(4 * (size_t)n);
+    b.idx_b = (uint32_t *)take(4 * (size_t)n);
+    b.radix_hist = (uint32_t *)take(4 * 256 * (size_t)b.radix_blocks);
+    b.radix_total = (uint32_t *)take(4 * 256);
+    b.ps = (float4 *)take(16 * (size_t)n);
+    b.lev_d = (int8_t *)take(n1);
+    b.lev_w = (int8_t *)take(n1);
+    b.ncount = (uint8_t *)take(n1);
+    b.pstart = (int32_t *)take(4 * n1);
+    b.node_start = (uint32_t *)take(4 * n1);
+    b.scan_partial = (uint32_t *)take(4 * (size_t)scan_partial_count((int64_t)n1));
+    b.meta = (int4 *)take(16 * (size_t)nodes);
+    b.parent = (int32_t *)take(4 * (size_t)nodes);
+    b.nchild = (int32_t *)take(4 * (size_t)nodes);
+    b.arrive = (int32_t *)take(4 * (size_t)nodes);
+    b.sums = (float4 *)take(16 * (size_t)nodes);
+    b.com = (float4 *)take(16 * (size_t)nodes);
+    b.acc_s = (float *)take(12 * (size_t)n);
+    b.cnt_s = (uint32_t *)take(12 * (size_t)n);
+    return off;
+}
+
+// Device address of this device's scratch, looked up once per device.
+int scratch_address(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return ORRERY_ECUDA;
+    }
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return ORRERY_ECUDA;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return ORRERY_OK;
+}
+
+}  // namespace
+}  // namespace obh
+
+using namespace obh;
+
+extern "C" int orrery_bh_forces_noalloc(const float *pos_d, const float *mass_d, int64_t n,
+                                        float theta, float eps, int32_t leaf_cap,
+                                        int32_t traversal, float *acc_d, uint32_t *interactions_d,
+                                        uint32_t *visits_d, void *stream)
+{
+    if (n < 0 || n > kMaxN || !(theta >= 0.0f) || !(eps >= 0.0f) || leaf_cap < 1 ||
+        (traversal != ORRERY_INDEPENDENT && traversal != ORRERY_COHERENT))
+        return ORRERY_EINVAL;
+    if (n == 0) return ORRERY_OK;
+    if (!pos_d || !mass_d || !acc_d) return ORRERY_EINVAL;
+    Buffers b{};
+    const int64_t nodes = bound_nodes(n, leaf_cap);
+    if (nodes > (int64_t)INT32_MAX || layout(b, nullptr, n, nodes) > kScratchBytes)
+        return ORRERY_ESCRATCH;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    void *base = nullptr;
+    int rc = scratch_address(&base);
+    if (rc != ORRERY_OK) return rc;
+    layout(b, (char *)base, n, nodes);
+    cudaStream_t st = (cudaStream_t)stream;
+    uint64_t *keys_sorted = nullptr;
+    uint32_t *perm = nullptr;
+    launch_bbox(pos_d, mass_d, b, st);
+    launch_morton(pos_d, b, st);
+    launch_sort(b, st, &keys_sorted, &perm);
+    launch_gather(pos_d, mass_d, perm, b, st);
+    launch_build(keys_sorted, leaf_cap, b, st);
+    launch_moments(leaf_cap, b, st);
+    launch_walk(traversal, theta, eps, leaf_cap, interactions_d != nullptr || visits_d != nullptr,
+                b, st);
+    launch_scatter(perm, b, acc_d, interactions_d, visits_d, st);
+    int status = 0;
+    cudaMemcpyAsync(&status, &b.params->status, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (cudaStreamSynchronize(st) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+        return ORRERY_ECUDA;
+    if (status & kStatusNonFinite) return ORRERY_ENONFINITE;
+    if (status & kStatusNodeBound) return ORRERY_ERANGE;
+    if (status & kStatusWalkBound) return ORRERY_EWALK;
+    if (status & kStatusInternal) return ORRERY_EINTERNAL;
+    return ORRERY_OK;
+}
