@@ -26,8 +26,9 @@
  *   moments:   leaf M = sum m, S = sum fma(m, x, S) in sorted order; internal
  *              nodes sum their children in order; CoM = S / M (0 if M <= 0)
  *   criterion: accept iff (side 2^-L)^2 < (theta^2) * |CoM - x_i|^2
- *   term:      r2 = |x_j - x_i|^2 + eps^2; f = m_j / (r2 sqrt(r2));
- *              a_i += f (x_j - x_i), fused multiply-add, in walk order
+ *   term:      r2 = |x_j - x_i|^2 + eps^2; y = the binary32 value nearest
+ *              1/sqrt(r2); f = (m_j y)(y y); a_i += f (x_j - x_i), fused
+ *              multiply-add, in walk order
  * Both traversals give bit-identical accelerations and counters.
  *
  * Memory: every pointer named *_d or documented "device" is a CUDA device
@@ -132,7 +133,7 @@ int orrery_bh_forces_host(const float *pos, const float *mass, int64_t n, float 
  * is one fixed 16 MiB array inside the library's device code, which every GPU
  * that loads the library holds until the process exits. A call fits iff its
  * buffers fit 16 MiB: at leaf_cap >= 16 every n <= 65536 fits; at leaf_cap 32
- * up to 96640 particles fit. A call that does not fit returns ORRERY_ESCRATCH
+ * up to 83968 particles fit. A call that does not fit returns ORRERY_ESCRATCH
  * before launching anything.
  *
  * The first call on each device looks up the array's device address (with

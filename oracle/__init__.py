@@ -101,6 +101,8 @@ def _bind(lib):
     lib.oracle_cube.restype = None
     lib.oracle_quantise.argtypes = [f32, f32, f32]
     lib.oracle_quantise.restype = ctypes.c_uint32
+    lib.oracle_rsqrt_rn.argtypes = [f32]
+    lib.oracle_rsqrt_rn.restype = f32
     lib.oracle_interleave.argtypes = [ctypes.c_uint32] * 3
     lib.oracle_interleave.restype = ctypes.c_uint64
     lib.oracle_keys.argtypes = [P, i64, P, f32, P]
@@ -161,6 +163,11 @@ def cube(pos) -> tuple[np.ndarray, np.float32, np.float32]:
 # --------------------------------------------------------------------------
 def quantise(x: float, lo: float, inv: float) -> int:
     return int(_load().oracle_quantise(float(x), float(lo), float(inv)))
+
+
+def rsqrt_rn(x: float) -> np.float32:
+    """The binary32 value nearest 1/sqrt(x) (the force term's inverse root)."""
+    return np.float32(_load().oracle_rsqrt_rn(float(np.float32(x))))
 
 
 def interleave(qx: int, qy: int, qz: int) -> int:

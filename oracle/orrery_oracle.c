@@ -23,9 +23,10 @@
  *   come from the workload definition that accompanies the pages.
  *
  * Precision. The pages measure single precision. Every floating-point step
- * below is one IEEE binary32 operation rounded to nearest-even: +, -, *, /,
- * sqrtf and fmaf (one rounding). The file is compiled with
- * -ffp-contract=off so the compiler adds no fused operations of its own.
+ * below is one binary32 operation rounded to nearest-even: +, -, *, /, fmaf
+ * (one rounding), and the inverse square root of the force term, which is
+ * the binary32 value nearest 1/sqrt(x) (oracle_rsqrt_rn). The file is
+ * compiled with -ffp-contract=off so the compiler adds no fused operations.
  * Where the pages leave the arithmetic open, the reading taken is written at
  * the step; the same readings are listed in the design notes.
  *
@@ -297,7 +298,8 @@ int oracle_moments(const float *ps, const int32_t *nodes, int64_t num_nodes, int
 /*                                                                          */
 /* Term for a source (x_j, m_j), Plummer softening, G = 1:                  */
 /*   r2 = fl(d2 + eps2), eps2 = fl(eps * eps)                               */
-/*   f  = fl(m_j / fl(r2 * sqrtf(r2)))                                      */
+/*   y  = rsqrt_rn(r2), the binary32 value nearest 1/sqrt(r2)               */
+/*   f  = fl(fl(m_j * y) * fl(y * y))       (m_j r2^(-3/2))                 */
 /*   a_ia = fmaf(f, dx_a, a_ia), in walk order                              */
 /* Cell terms use (M, CoM) with the d2 of the acceptance test.              */
 /*                                                                          */
@@ -322,6 +324,29 @@ static float cell_side_sq(float side, int level)
     return ldexpf(side * side, -2 * level);
 }
 
+/* The binary32 value nearest to 1/sqrt(x) (round to nearest; no ties can
+ * occur: a midpoint between floats has 25 significant bits, and 1/m^2 of
+ * such an m is never a binary32 value). A double estimate is within one ulp
+ * of it; the two neighbouring midpoints m then decide exactly, since
+ * 1/sqrt(x) > m  <=>  m*m*x < 1, and m*m is exact in double while fma gives
+ * the sign of m*m*x - 1 exactly. Special values: +-0 -> +-inf, +inf -> +0,
+ * negative or NaN -> NaN. */
+float oracle_rsqrt_rn(float x)
+{
+    if (isnan(x) || x < 0.0f) return NAN;
+    if (x == 0.0f) return copysignf(INFINITY, x);
+    if (isinf(x)) return 0.0f;
+    float y = (float)(1.0 / sqrt((double)x));
+    const double xd = (double)x;
+    float up = nextafterf(y, INFINITY);
+    double mid = 0.5 * ((double)y + (double)up);
+    if (fma(mid * mid, xd, -1.0) < 0.0) return up;
+    float down = nextafterf(y, 0.0f);
+    mid = 0.5 * ((double)y + (double)down);
+    if (fma(mid * mid, xd, -1.0) > 0.0) return down;
+    return y;
+}
+
 static void add_term(const float xi[3], float xj, float yj, float zj, float m, float eps2,
                      float acc[3])
 {
@@ -330,7 +355,8 @@ static void add_term(const float xi[3], float xj, float yj, float zj, float m, f
     float dz = zj - xi[2];
     float d2 = fmaf(dz, dz, fmaf(dy, dy, dx * dx));
     float r2 = d2 + eps2;
-    float f = m / (r2 * sqrtf(r2));
+    float y = oracle_rsqrt_rn(r2);
+    float f = (m * y) * (y * y);
     acc[0] = fmaf(f, dx, acc[0]);
     acc[1] = fmaf(f, dy, acc[1]);
     acc[2] = fmaf(f, dz, acc[2]);

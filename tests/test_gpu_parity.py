@@ -148,6 +148,34 @@ def test_forces_theta_sweep(tt, name, theta):
         check_forces(tt, pos, mass, cap, T, theta, traversal)
 
 
+@pytest.mark.parametrize("eps", [0.0, 1e-20, 0.5])
+@pytest.mark.parametrize("name", ["ragged_5003_cap7", "unequal_masses_cap16"])
+def test_forces_softening_sweep(tt, name, eps):
+    # eps = 0 and a denormal eps^2 take the kernels' per-particle self check
+    # (the self term would not be finite); eps = 0.5 the self-term-free loop
+    pos, mass, cap, T = case(name)
+    for traversal in ("coherent", "independent"):
+        acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), 0.5, eps, cap, traversal)
+        r_acc, r_pc, r_pp, r_vis = T.walk(0.5, eps, threads=oracle.default_threads())
+        g = acc.cpu().numpy()[T.perm]
+        assert np.array_equal(g.view(np.uint32), r_acc.view(np.uint32))
+        g_inter = u32(inter)[T.perm]
+        assert np.array_equal(g_inter[:, 0], r_pc) and np.array_equal(g_inter[:, 1], r_pp)
+
+
+def test_coincident_points_without_softening(tt):
+    # r2 = 0 between coincident points: y = +inf and the term is NaN on both
+    # sides (the softened law is singular there); the counts still agree
+    pos, mass, cap, T = case("duplicates_65")
+    acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), 0.5, 0.0, cap, "coherent")
+    r_acc, r_pc, r_pp, r_vis = T.walk(0.5, 0.0)
+    g = acc.cpu().numpy()[T.perm]
+    assert np.array_equal(np.isnan(g), np.isnan(r_acc))
+    ok = ~np.isnan(r_acc)
+    assert np.array_equal(g[ok].view(np.uint32), r_acc[ok].view(np.uint32))
+    assert np.array_equal(u32(inter)[T.perm][:, 1], r_pp)
+
+
 def test_empty_input(tt):
     acc, inter, vis = tt.bh_forces(torch.zeros((0, 3), device="cuda"), torch.zeros(0, device="cuda"))
     assert acc.shape == (0, 3)

@@ -160,6 +160,35 @@ def test_interleave_single_bits():
     pin_interleave_single_bits()
 
 
+def pin_rsqrt_rn():
+    """The term's inverse root is the binary32 value nearest 1/sqrt(x): checked
+    exactly with rationals (y is nearest iff the squared half-ulp midpoints on
+    either side bracket 1/x)."""
+    from fractions import Fraction
+
+    rng = np.random.default_rng(11)
+    xs = np.concatenate([
+        rng.uniform(0.0025, 100.0, 3000), 10.0 ** rng.uniform(-44, 38, 3000),
+        [1.0, 2.0, 4.0, 0.25, 3.0, 1e-45, 1.17549435e-38, 3.4028235e38, 0.0025],
+    ]).astype(np.float32)
+    for x in xs:
+        if x <= 0:
+            continue
+        y = oracle.rsqrt_rn(x)
+        up = np.nextafter(y, np.float32(np.inf))
+        down = np.nextafter(y, np.float32(0))
+        X = Fraction(float(x))
+        hi = (Fraction(float(y)) + Fraction(float(up))) / 2
+        lo = (Fraction(float(y)) + Fraction(float(down))) / 2
+        assert hi * hi * X > 1 and lo * lo * X < 1, float(x)
+    assert oracle.rsqrt_rn(0.0) == np.inf and oracle.rsqrt_rn(-0.0) == -np.inf
+    assert oracle.rsqrt_rn(np.inf) == 0.0 and np.isnan(oracle.rsqrt_rn(-1.0))
+
+
+def test_rsqrt_is_correctly_rounded():
+    pin_rsqrt_rn()
+
+
 def test_quantise_floor_and_clamp():
     inv = np.float32(2 ** 21)  # side 1
     assert oracle.quantise(0.0, 0.0, inv) == 0
@@ -526,6 +555,11 @@ MISTAKES = [
      "return cell_side_sq(side, level) <= theta2 * d2;", pin_degenerate),
     ("last lane dropped from the union", "i < (g + 1) * width && i < n",
      "i < (g + 1) * width - 1 && i < n", pin_group_union),
+    ("inverse root midpoint test reversed", "if (fma(mid * mid, xd, -1.0) < 0.0) return up;",
+     "if (fma(mid * mid, xd, -1.0) > 0.0) return up;", pin_rsqrt_rn),
+    ("inverse root as 1/sqrtf without correction",
+     "float y = (float)(1.0 / sqrt((double)x));\n    const double xd = (double)x;",
+     "return 1.0f / sqrtf(x);\n    float y = 0; const double xd = (double)x;", pin_rsqrt_rn),
     ("cell term uses the target's mass", "add_term(xi, c[0], c[1], c[2], c[3], eps2, acc);",
      "add_term(xi, c[0], c[1], c[2], t->ps[4 * i + 3], eps2, acc);", pin_far_clump),
 ]

@@ -106,6 +106,7 @@ size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
     b.arrive = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
     b.sums = (float4 *)take(sizeof(float4) * (size_t)nodes);
     b.com = (float4 *)take(sizeof(float4) * (size_t)nodes);
+    b.wnode = (int4 *)take(sizeof(int4) * (size_t)nodes);
     b.acc_s = (float *)take(sizeof(float) * 3 * (size_t)n);
     b.cnt_s = (uint32_t *)take(sizeof(uint32_t) * 3 * (size_t)n);
     return off;

@@ -140,6 +140,16 @@ __device__ __forceinline__ void store_moments(int64_t k, float sx, float sy, flo
     __stcg(com + k, c);
 }
 
+// Stores a node's moments and its walk record {escape, first, leaf count
+// (0 for an internal node), bits of (side 2^-level)^2}.
+__device__ __forceinline__ void store_node(int64_t k, const int4 &m, bool leaf, float sx, float sy,
+                                           float sz, float M, float4 *sums, float4 *com,
+                                           int4 *wnode, const DeviceParams *P)
+{
+    wnode[k] = make_int4(m.x, m.y, leaf ? m.z : 0, __float_as_int(P->s2[m.w]));
+    store_moments(k, sx, sy, sz, M, sums, com);
+}
+
 // a6: one thread per leaf (the last node of each position's chain) sums its
 // particles in sorted order, then climbs: the last child to arrive at a
 // parent (atomic arrival count == child count) sums all of the parent's
@@ -148,7 +158,8 @@ __global__ void __launch_bounds__(kThreads)
 k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ ncount,
           const uint32_t *__restrict__ node_start, const int4 *__restrict__ meta,
           const int32_t *__restrict__ parent, const int32_t *__restrict__ nchild,
-          int32_t *__restrict__ arrive, float4 *sums, float4 *com, DeviceParams *P)
+          int32_t *__restrict__ arrive, float4 *sums, float4 *com, int4 *__restrict__ wnode,
+          DeviceParams *P)
 {
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
@@ -169,7 +180,7 @@ k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ 
         sy = __fmaf_rn(p.w, p.y, sy);
         sz = __fmaf_rn(p.w, p.z, sz);
     }
-    store_moments(k, sx, sy, sz, M, sums, com);
+    store_node(k, m, true, sx, sy, sz, M, sums, com, wnode, P);
     int64_t node = parent[k];
     while (node >= 0) {
         __threadfence();
@@ -195,7 +206,7 @@ k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ 
             }
             c = nc;
         }
-        store_moments(node, sx, sy, sz, M, sums, com);
+        store_node(node, meta[node], false, sx, sy, sz, M, sums, com, wnode, P);
         node = parent[node];
     }
 }
@@ -223,7 +234,7 @@ void launch_moments(int32_t leaf_cap, const Buffers &b, cudaStream_t st)
     cudaMemsetAsync(b.arrive, 0, sizeof(int32_t) * (size_t)b.max_nodes, st);
     k_moments<<<ceil_div(b.n, kThreads), kThreads, 0, st>>>(b.ps, b.n, b.ncount, b.node_start,
                                                            b.meta, b.parent, b.nchild, b.arrive,
-                                                           b.sums, b.com, b.params);
+                                                           b.sums, b.com, b.wnode, b.params);
     g_launches += 1;
 }
 

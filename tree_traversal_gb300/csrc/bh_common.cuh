@@ -24,10 +24,10 @@ struct DeviceParams {
     float side;
     float inv;
     float s2[kLevels + 1];  // (side * 2^-L)^2 for L = 0..21
+    float mmax;             // largest |m|: bounds the self term (see the walk)
     int status;
     int num_nodes;
     int depth;
-    int pad;
 };
 
 // Device pointers carved out of one workspace allocation.
@@ -60,6 +60,8 @@ struct Buffers {
     // a6
     float4 *sums;             // [max_nodes] {S_x, S_y, S_z, M}
     float4 *com;              // [max_nodes] {CoM_x, CoM_y, CoM_z, M}
+    int4 *wnode;              // [max_nodes] walk record {escape, first, leaf count or 0,
+                              //  bits of the node's squared side}
     // a7
     float *acc_s;             // [n][3] sorted order
     uint32_t *cnt_s;          // [n][3] {pc, pp, visits} sorted order

@@ -27,37 +27,24 @@ __device__ __forceinline__ void warp_minmax(float &lo, float &hi)
     }
 }
 
-// a1, part 1: per-block min / max per axis and a non-finite flag.
-__global__ void __launch_bounds__(kBBoxThreads)
-k_bbox_partial(const float *__restrict__ pos, const float *__restrict__ mass, int64_t n,
-               float *__restrict__ partial)
+// Folds one value set per thread over the block; thread 0 writes
+// {lo[3], hi[3], bad, mmax} to out.
+__device__ __forceinline__ void block_fold(float lo[3], float hi[3], float mmax, int bad, float *out)
 {
-    float lo[3] = {INFINITY, INFINITY, INFINITY};
-    float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
-    int bad = 0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        float m = __ldg(mass + i);
-        bad |= !isfinite(m);
-#pragma unroll
-        for (int a = 0; a < 3; ++a) {
-            float x = __ldg(pos + 3 * i + a);
-            bad |= !isfinite(x);
-            lo[a] = fminf(lo[a], x);
-            hi[a] = fmaxf(hi[a], x);
-        }
-    }
     __shared__ float s_lo[3][kBBoxThreads / 32], s_hi[3][kBBoxThreads / 32];
+    __shared__ float s_m[kBBoxThreads / 32];
     __shared__ int s_bad[kBBoxThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int a = 0; a < 3; ++a) warp_minmax(lo[a], hi[a]);
+    for (int off = 16; off > 0; off >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, off));
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
         for (int a = 0; a < 3; ++a) {
             s_lo[a][warp] = lo[a];
             s_hi[a][warp] = hi[a];
         }
+        s_m[warp] = mmax;
         s_bad[warp] = bad;
     }
     __syncthreads();
@@ -67,35 +54,73 @@ k_bbox_partial(const float *__restrict__ pos, const float *__restrict__ mass, in
                 lo[a] = fminf(lo[a], s_lo[a][w]);
                 hi[a] = fmaxf(hi[a], s_hi[a][w]);
             }
+            mmax = fmaxf(mmax, s_m[w]);
             bad |= s_bad[w];
         }
-        float *o = partial + 8 * blockIdx.x;
         for (int a = 0; a < 3; ++a) {
-            o[a] = lo[a];
-            o[3 + a] = hi[a];
+            out[a] = lo[a];
+            out[3 + a] = hi[a];
         }
-        o[6] = bad ? 1.0f : 0.0f;
+        out[6] = bad ? 1.0f : 0.0f;
+        out[7] = mmax;
     }
+}
+
+// a1, part 1: per-block min / max per axis, max |m| and a non-finite flag.
+__global__ void __launch_bounds__(kBBoxThreads)
+k_bbox_partial(const float *__restrict__ pos, const float *__restrict__ mass, int64_t n,
+               float *__restrict__ partial)
+{
+    float lo[3] = {INFINITY, INFINITY, INFINITY};
+    float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
+    float mmax = 0.0f;
+    int bad = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float m = __ldg(mass + i);
+        bad |= !isfinite(m);
+        mmax = fmaxf(mmax, fabsf(m));
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+            float x = __ldg(pos + 3 * i + a);
+            bad |= !isfinite(x);
+            lo[a] = fminf(lo[a], x);
+            hi[a] = fmaxf(hi[a], x);
+        }
+    }
+    block_fold(lo, hi, mmax, bad, partial + 8 * blockIdx.x);
 }
 
 // a1, part 2: one block folds the partials and derives the cube:
 // side = max_a (hi_a - lo_a), inv = 2^21 / side, and the per-level squared
 // cell side s2[L] = (side * side) * 2^(-2L) (an exact power-of-two scaling).
 // Also resets the status word, node count and depth of this evaluation.
-__global__ void k_bbox_final(const float *__restrict__ partial, int blocks, DeviceParams *P)
+__global__ void __launch_bounds__(kBBoxThreads)
+k_bbox_final(const float *__restrict__ partial, int blocks, DeviceParams *P)
 {
-    if (threadIdx.x != 0) return;
+    __shared__ float s_out[8];
     float lo[3] = {INFINITY, INFINITY, INFINITY};
     float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
+    float mmax = 0.0f;
     int bad = 0;
-    for (int b = 0; b < blocks; ++b) {
+    for (int b = threadIdx.x; b < blocks; b += blockDim.x) {
         const float *o = partial + 8 * b;
         for (int a = 0; a < 3; ++a) {
             lo[a] = fminf(lo[a], o[a]);
             hi[a] = fmaxf(hi[a], o[3 + a]);
         }
         bad |= (o[6] != 0.0f);
+        mmax = fmaxf(mmax, o[7]);
     }
+    block_fold(lo, hi, mmax, bad, s_out);
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    for (int a = 0; a < 3; ++a) {
+        lo[a] = s_out[a];
+        hi[a] = s_out[3 + a];
+    }
+    bad = s_out[6] != 0.0f;
+    P->mmax = s_out[7];
     float side = 0.0f;
     for (int a = 0; a < 3; ++a) {
         float ext = __fsub_rn(hi[a], lo[a]);
@@ -299,7 +324,7 @@ void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *p
 void launch_bbox(const float *pos, const float *mass, const Buffers &b, cudaStream_t st)
 {
     k_bbox_partial<<<b.bbox_blocks, kBBoxThreads, 0, st>>>(pos, mass, b.n, b.bbox_partial);
-    k_bbox_final<<<1, 32, 0, st>>>(b.bbox_partial, b.bbox_blocks, b.params);
+    k_bbox_final<<<1, kBBoxThreads, 0, st>>>(b.bbox_partial, b.bbox_blocks, b.params);
     g_launches += 2;
 }
 
