@@ -44,7 +44,8 @@ def parse():
     p.add_argument("--steps", type=int, default=11)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--workload", default="plummer_1048576")
-    p.add_argument("--traversal", default="coherent", choices=["coherent", "independent"])
+    p.add_argument("--traversal", default="coherent",
+                   choices=["coherent", "coherent16", "coherent64", "independent"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=8.0,
                    help="target wall time of the CPU-oracle sample")
@@ -235,7 +236,7 @@ def main():
                                      trav, out=(acc, inter, visits))
 
     # untimed: the comparison traversal (its visits give the redundancy ratio)
-    other = "independent" if args.traversal == "coherent" else "coherent"
+    other = "independent" if args.traversal != "independent" else "coherent"
     call(other)
     t_other = tt.last_timings()
     vis_other = visits.double().mean().item()
@@ -329,8 +330,8 @@ def main():
         "gpu_launches": int(launches),
         "clocks": {"sm_mhz": csum["sm_mhz"], "sm_max_mhz": csum["sm_max_mhz"],
                    "reasons": csum["reasons"]},
-        "roofline": {"bound": "alu", "kernel": "k_walk_coherent" if args.traversal == "coherent"
-                     else "k_walk_independent",
+        "roofline": {"bound": "alu", "kernel": "k_walk_independent"
+                     if args.traversal == "independent" else "k_walk_coherent",
                      "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / peak_tflops, "traffic": traffic,
                      "peak_basis": "%d SMs x %d FP32 lanes x 2 flop x %.0f MHz (max SM clock of "
@@ -356,7 +357,7 @@ def main():
         "tree": {"num_nodes": phases[-1]["num_nodes"], "depth": phases[-1]["depth"]},
         "per_particle": {"interactions": interactions / n, "cells": pc_mean, "particles": pp_mean,
                          "visits": vis_mean, "visits_" + other: vis_other,
-                         "redundancy": (vis_mean / vis_other) if args.traversal == "coherent"
+                         "redundancy": (vis_mean / vis_other) if args.traversal != "independent"
                          else (vis_other / vis_mean)},
         "walk_ms_" + other: t_other["walk_ms"],
     }

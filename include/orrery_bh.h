@@ -62,10 +62,15 @@ extern "C" {
                                   its fixed scratch array */
 
 /* Which traversal the walk kernel runs ("sycl_tree_solver.hpp",
- * TreeTraversal). Both compute the same function of the input. */
+ * TreeTraversal). All compute the same function of the input; the coherent
+ * ones differ only in how many consecutive sorted targets share one node
+ * index (the coherence width; docs/performance/sycl_tree.md, "The sub-group
+ * width"), which changes the visit counts they report and their speed. */
 typedef enum {
-    ORRERY_INDEPENDENT = 0, /* one thread per target, each on its own node index */
-    ORRERY_COHERENT = 1     /* one node index per warp, advanced by min over lanes */
+    ORRERY_INDEPENDENT = 0,  /* one thread per target, each on its own node index */
+    ORRERY_COHERENT = 1,     /* 32 targets (one warp) share a node index */
+    ORRERY_COHERENT_16 = 2,  /* 16 targets (half a warp) share a node index */
+    ORRERY_COHERENT_64 = 3   /* 64 targets (one warp, two per lane) share a node index */
 } orrery_traversal;
 
 /* Where the last evaluation spent its time ("sycl_tree_solver.hpp",
@@ -97,13 +102,14 @@ typedef struct {
  *   theta        opening angle, >= 0 (0 opens every cell: direct summation)
  *   eps          Plummer softening length, >= 0
  *   leaf_cap     >= 1: a cell holding at most this many particles is a leaf
- *   traversal    ORRERY_INDEPENDENT or ORRERY_COHERENT
+ *   traversal    an orrery_traversal value
  *   acc_d        device, float32 [n][3], written in the caller's order
  *   interactions_d  device, uint32 [n][2] {particle-cell, particle-particle}
  *                per target in the caller's order, or NULL
  *   visits_d     device, uint32 [n] node visits per target, or NULL. For the
- *                independent walk a target's own walk; for the coherent walk
- *                the size of its warp's union (32 consecutive sorted targets)
+ *                independent walk a target's own walk; for a coherent walk
+ *                the size of the union of its group's walks (the group =
+ *                16, 32 or 64 consecutive sorted targets)
  *   stream       cudaStream_t
  * Returns ORRERY_OK or a negative status.
  */

@@ -25,6 +25,8 @@ from inputs import PAGES_SEED, plummer, two_spheres, uniform_cube
 pytestmark = pytest.mark.gpu
 EPS = 0.05
 REL_TOL = 1e-5
+WIDTH = {"coherent": 32, "coherent16": 16, "coherent64": 64}
+TRAVERSALS = ["coherent", "independent", "coherent16", "coherent64"]
 
 
 @pytest.fixture(scope="module")
@@ -127,13 +129,14 @@ def check_forces(tt, pos, mass, cap, T, theta, traversal):
     if traversal == "independent":
         want = r_vis
     else:
-        want = np.repeat(T.group_visits(theta, EPS, 32), 32)[: T.n]
+        width = WIDTH[traversal]
+        want = np.repeat(T.group_visits(theta, EPS, width), width)[: T.n]
     assert np.array_equal(u32(vis)[inv], want)
     t = tt.last_timings()
     assert t["num_nodes"] == T.num_nodes and t["depth"] == T.depth and t["n"] == T.n
 
 
-@pytest.mark.parametrize("traversal", ["coherent", "independent"])
+@pytest.mark.parametrize("traversal", TRAVERSALS)
 @pytest.mark.parametrize("name", list(CASES))
 def test_forces_bit_exact(tt, name, traversal):
     pos, mass, cap, T = case(name)
@@ -144,7 +147,7 @@ def test_forces_bit_exact(tt, name, traversal):
 @pytest.mark.parametrize("name", ["ragged_5003_cap7", "duplicates_65", "grid_ties_cap4"])
 def test_forces_theta_sweep(tt, name, theta):
     pos, mass, cap, T = case(name)
-    for traversal in ("coherent", "independent"):
+    for traversal in TRAVERSALS:
         check_forces(tt, pos, mass, cap, T, theta, traversal)
 
 
@@ -154,7 +157,7 @@ def test_forces_softening_sweep(tt, name, eps):
     # eps = 0 and a denormal eps^2 take the kernels' per-particle self check
     # (the self term would not be finite); eps = 0.5 the self-term-free loop
     pos, mass, cap, T = case(name)
-    for traversal in ("coherent", "independent"):
+    for traversal in TRAVERSALS:
         acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), 0.5, eps, cap, traversal)
         r_acc, r_pc, r_pp, r_vis = T.walk(0.5, eps, threads=oracle.default_threads())
         g = acc.cpu().numpy()[T.perm]
@@ -288,6 +291,14 @@ def check_full_size(tt, pos, mass, thetas, cap=32):
         assert np.array_equal(u32(v_ind)[caller], r_vis)
         union = T.group_visits(theta, EPS, 32, warps)
         assert np.array_equal(u32(vis)[caller], np.repeat(union, [min(32, T.n - 32 * w) for w in warps]))
+        # width 64: same sums and counts, visits = the 64-target group's union
+        a64, i64, v64 = tt.bh_forces(p, m, theta, EPS, cap, "coherent64")
+        assert torch.equal(a64.view(torch.int32), acc.view(torch.int32)) and torch.equal(i64, inter)
+        g64 = np.unique(warps // 2)
+        u64 = T.group_visits(theta, EPS, 64, g64)
+        t64 = np.concatenate([np.arange(64 * g, min(T.n, 64 * g + 64)) for g in g64])
+        assert np.array_equal(u32(v64)[T.perm[t64]],
+                              np.repeat(u64, [min(64, T.n - 64 * g) for g in g64]))
 
 
 def test_full_size_plummer_1m(tt):

@@ -26,6 +26,10 @@ ESCRATCH = -8
 
 INDEPENDENT = 0
 COHERENT = 1
+COHERENT_16 = 2
+COHERENT_64 = 3
+# coherence width of each traversal (targets sharing one node index)
+WIDTH = {INDEPENDENT: 1, COHERENT: 32, COHERENT_16: 16, COHERENT_64: 64}
 
 
 class Timings(ctypes.Structure):

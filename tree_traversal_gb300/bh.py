@@ -14,14 +14,16 @@ import torch
 from . import _lib
 
 _TRAVERSALS = {"independent": _lib.INDEPENDENT, "coherent": _lib.COHERENT,
-               _lib.INDEPENDENT: _lib.INDEPENDENT, _lib.COHERENT: _lib.COHERENT}
+               "coherent16": _lib.COHERENT_16, "coherent64": _lib.COHERENT_64}
+_TRAVERSALS.update({v: v for v in list(_TRAVERSALS.values())})
 
 
 def _traversal(t) -> int:
     try:
         return _TRAVERSALS[t]
     except KeyError:
-        raise ValueError("traversal must be 'independent' or 'coherent', got %r" % (t,)) from None
+        raise ValueError("traversal must be one of %s, got %r"
+                         % (sorted(k for k in _TRAVERSALS if isinstance(k, str)), t)) from None
 
 
 def _check_device(t: torch.Tensor, name: str, shape, dtype=torch.float32):

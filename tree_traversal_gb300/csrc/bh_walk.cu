@@ -37,6 +37,8 @@
 // signs). The factor is finite iff eps > 0 and (m_max y)(y y) does not
 // overflow for y = rsqrt(eps^2); the kernels test that once per block and
 // drop the per-particle self comparison when it holds.
+#include <type_traits>
+
 #include "bh_common.cuh"
 
 namespace obh {
@@ -105,88 +107,175 @@ __device__ __forceinline__ bool prologue(const WalkArgs &a, int &num_nodes, bool
     return s_state[0] == 0;
 }
 
-template <bool kCount, bool kSelfFree>
+// One coherence group = W consecutive sorted targets sharing one node index.
+// W = 16: half a warp per group (two groups per warp, each advancing on its
+// own, as the pages' sub-group width of 16); W = 32: one warp; W = 64: one
+// warp with two targets per lane (the width the pages could not measure).
+// Lanes hold targets base + i*G + lane for i < T, where G = lanes per group
+// and T = targets per lane.
+template <int W>
+struct Group {
+    static constexpr int G = W < 32 ? W : 32;
+    static constexpr int T = W > 32 ? W / 32 : 1;
+};
+
+// Cell or particle term with a per-target predicate: a target that does not
+// take the term gets f = 0, and fma(0, d, a) = a exactly (d is finite and a
+// is never -0), so masking by selection leaves its sum bit-identical.
+__device__ __forceinline__ void masked_term(bool take, float dx, float dy, float dz, float d2,
+                                            float m, float eps2, float &ax, float &ay, float &az)
+{
+    const float r2 = __fadd_rn(d2, eps2);
+    const float y = __frsqrt_rn(r2);
+    float f = __fmul_rn(__fmul_rn(m, y), __fmul_rn(y, y));
+    f = take ? f : 0.0f;
+    ax = __fmaf_rn(f, dx, ax);
+    ay = __fmaf_rn(f, dy, ay);
+    az = __fmaf_rn(f, dz, az);
+}
+
+template <int W, bool kCount, bool kSelfFree>
 __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, float4 *stage)
 {
+    constexpr int G = Group<W>::G;
+    constexpr int T = Group<W>::T;
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kThreads + threadIdx.x;
-    const bool valid = t < a.n;
-    const float4 xi = valid ? __ldg(a.ps + t) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    int next = valid ? 0 : num_nodes;
-    float ax = 0.0f, ay = 0.0f, az = 0.0f;
-    uint32_t pc = 0, pp = 0;
+    const int glane = lane & (G - 1);
+    const unsigned gmask = (G == 32) ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
+    const int gid = (blockIdx.x * kThreads + threadIdx.x) / G;  // group index
+    const int base = gid * W;
+
+    int tgt[T], next[T];
+    bool valid[T];
+    float4 xi[T];
+    float ax[T], ay[T], az[T];
+    uint32_t pc[T], pp[T];
+#pragma unroll
+    for (int i = 0; i < T; ++i) {
+        tgt[i] = base + i * G + glane;
+        valid[i] = tgt[i] < a.n;
+        xi[i] = valid[i] ? __ldg(a.ps + tgt[i]) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        next[i] = valid[i] ? 0 : num_nodes;
+        ax[i] = ay[i] = az[i] = 0.0f;
+        pc[i] = pp[i] = 0;
+    }
+    auto group_min = [&]() {
+        int v = next[0];
+#pragma unroll
+        for (int i = 1; i < T; ++i) v = min(v, next[i]);
+        return __reduce_min_sync(gmask, v);
+    };
+    int k = group_min();
+    float4 c = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int4 w = make_int4(0, 0, 0, 0);
+    if (k < num_nodes) {
+        c = __ldg(a.com + k);
+        w = __ldg(a.wnode + k);
+    }
     int steps = 0;
-    for (; steps <= num_nodes; ++steps) {
-        const int k = __reduce_min_sync(0xffffffffu, next);
-        if (k >= num_nodes) break;
-        const float4 c = __ldg(a.com + k);
-        const int4 w = __ldg(a.wnode + k);
-        bool open = false;
-        if (next == k) {
-            const float dx = __fsub_rn(c.x, xi.x);
-            const float dy = __fsub_rn(c.y, xi.y);
-            const float dz = __fsub_rn(c.z, xi.z);
-            const float d2 = dist2(dx, dy, dz);
-            if (__int_as_float(w.w) < __fmul_rn(a.theta2, d2)) {
-                add_term(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
-                if (kCount) ++pc;
-                next = w.x;
-            } else {
-                open = w.z != 0;
-                next = open ? w.x : k + 1;
-            }
+    for (; k < num_nodes && steps <= num_nodes; ++steps) {
+        // the next node is k + 1 whenever any lane descends (and after every
+        // leaf): start its loads now, ahead of this step's arithmetic
+        const int kp = min(k + 1, num_nodes - 1);
+        const float4 cp = __ldg(a.com + kp);
+        const int4 wp = __ldg(a.wnode + kp);
+
+        const float side2 = __int_as_float(w.w);
+        const bool leaf = w.z != 0;
+        bool acc[T], open[T];
+        float dx[T], dy[T], dz[T], d2[T];
+        bool any_acc = false, any_open = false;
+#pragma unroll
+        for (int i = 0; i < T; ++i) {
+            const bool act = next[i] == k;
+            dx[i] = __fsub_rn(c.x, xi[i].x);
+            dy[i] = __fsub_rn(c.y, xi[i].y);
+            dz[i] = __fsub_rn(c.z, xi[i].z);
+            d2[i] = dist2(dx[i], dy[i], dz[i]);
+            acc[i] = act && side2 < __fmul_rn(a.theta2, d2[i]);
+            open[i] = act && !acc[i] && leaf;
+            next[i] = act ? ((acc[i] || leaf) ? w.x : k + 1) : next[i];
+            if (kCount) pc[i] += acc[i] ? 1u : 0u;
+            any_acc |= acc[i];
+            any_open |= open[i];
         }
-        if (__any_sync(0xffffffffu, open)) {
+        if (__any_sync(gmask, any_acc)) {
+#pragma unroll
+            for (int i = 0; i < T; ++i)
+                masked_term(acc[i], dx[i], dy[i], dz[i], d2[i], c.w, a.eps2, ax[i], ay[i], az[i]);
+        }
+        if (__any_sync(gmask, any_open)) {
             const int first = w.y, count = w.z;
-            if (first < 0 || first > a.n - count) {  // warp-uniform consistency check
-                if (lane == 0) atomicOr(&a.P->status, kStatusInternal);
+            if (first < 0 || first > a.n - count) {  // group-uniform consistency check
+                if (glane == 0) atomicOr(&a.P->status, kStatusInternal);
                 break;
             }
-            if (kCount && open) pp += count - ((unsigned)(t - first) < (unsigned)count ? 1u : 0u);
-            for (int base = 0; base < count; base += 32) {
-                const int chunk = min(32, count - base);
-                if (lane < chunk) stage[lane] = __ldg(a.ps + first + base + lane);
-                __syncwarp();
-                if (open) {
-                    if (kSelfFree) {
-#pragma unroll 4
-                        for (int j = 0; j < chunk; ++j)
-                            particle_term(stage[j], xi, a.eps2, ax, ay, az);
-                    } else {
-                        const int self = t - (first + base);
-                        for (int j = 0; j < chunk; ++j)
-                            if (j != self) particle_term(stage[j], xi, a.eps2, ax, ay, az);
+            if (kCount) {
+#pragma unroll
+                for (int i = 0; i < T; ++i)
+                    pp[i] += open[i] ? count - ((unsigned)(tgt[i] - first) < (unsigned)count ? 1u : 0u)
+                                     : 0u;
+            }
+            for (int b = 0; b < count; b += G) {
+                const int chunk = min(G, count - b);
+                if (glane < chunk) stage[glane] = __ldg(a.ps + first + b + glane);
+                __syncwarp(gmask);
+#pragma unroll 2
+                for (int j = 0; j < chunk; ++j) {
+                    const float4 p = stage[j];
+#pragma unroll
+                    for (int i = 0; i < T; ++i) {
+                        const bool take = kSelfFree ? open[i] : (open[i] && first + b + j != tgt[i]);
+                        const float ex = __fsub_rn(p.x, xi[i].x);
+                        const float ey = __fsub_rn(p.y, xi[i].y);
+                        const float ez = __fsub_rn(p.z, xi[i].z);
+                        masked_term(take, ex, ey, ez, dist2(ex, ey, ez), p.w, a.eps2, ax[i], ay[i],
+                                    az[i]);
                     }
                 }
-                __syncwarp();
+                __syncwarp(gmask);
             }
         }
+        const int k2 = group_min();
+        if (k2 == k + 1) {
+            c = cp;
+            w = wp;
+        } else if (k2 < num_nodes) {
+            c = __ldg(a.com + k2);
+            w = __ldg(a.wnode + k2);
+        }
+        k = k2;
     }
-    if (steps > num_nodes && lane == 0) atomicOr(&a.P->status, kStatusWalkBound);
-    if (valid) {
-        a.acc_s[3 * (int64_t)t + 0] = ax;
-        a.acc_s[3 * (int64_t)t + 1] = ay;
-        a.acc_s[3 * (int64_t)t + 2] = az;
+    if (k < num_nodes && glane == 0) atomicOr(&a.P->status, kStatusWalkBound);
+#pragma unroll
+    for (int i = 0; i < T; ++i) {
+        if (!valid[i]) continue;
+        const int64_t t = tgt[i];
+        a.acc_s[3 * t + 0] = ax[i];
+        a.acc_s[3 * t + 1] = ay[i];
+        a.acc_s[3 * t + 2] = az[i];
         if (kCount) {
-            a.cnt_s[3 * (int64_t)t + 0] = pc;
-            a.cnt_s[3 * (int64_t)t + 1] = pp;
-            a.cnt_s[3 * (int64_t)t + 2] = (uint32_t)steps;  // every step visits the union
+            a.cnt_s[3 * t + 0] = pc[i];
+            a.cnt_s[3 * t + 1] = pp[i];
+            a.cnt_s[3 * t + 2] = (uint32_t)steps;  // every step visits the group's union
         }
     }
 }
 
-template <bool kCount>
+template <int W, bool kCount>
 __global__ void __launch_bounds__(kThreads) k_walk_coherent(WalkArgs a)
 {
     __shared__ float4 s_leaf[kWarpsPerBlock][32];
     int num_nodes;
     bool self_free;
     if (!prologue(a, num_nodes, self_free)) return;  // block-uniform
-    float4 *stage = s_leaf[threadIdx.x >> 5];
+    const int lane = threadIdx.x & 31;
+    constexpr int G = Group<W>::G;
+    float4 *stage = &s_leaf[threadIdx.x >> 5][lane & ~(G - 1)];
     if (self_free)
-        coherent_walk<kCount, true>(a, num_nodes, stage);
+        coherent_walk<W, kCount, true>(a, num_nodes, stage);
     else
-        coherent_walk<kCount, false>(a, num_nodes, stage);
+        coherent_walk<W, kCount, false>(a, num_nodes, stage);
 }
 
 template <bool kCount, bool kSelfFree>
@@ -263,12 +352,20 @@ void launch_walk(int traversal, float theta, float eps, int32_t leaf_cap, bool c
     a.acc_s = b.acc_s;
     a.cnt_s = b.cnt_s;
     const unsigned grid = ceil_div(b.n, kThreads);
-    if (traversal == 1) {
+    // coherent groups of W targets: kThreads lanes cover kThreads * T targets
+    auto coherent = [&](auto wtag) {
+        constexpr int W = decltype(wtag)::value;
+        const unsigned g = ceil_div(b.n, (int64_t)kThreads * Group<W>::T);
         if (count)
-            k_walk_coherent<true><<<grid, kThreads, 0, st>>>(a);
+            k_walk_coherent<W, true><<<g, kThreads, 0, st>>>(a);
         else
-            k_walk_coherent<false><<<grid, kThreads, 0, st>>>(a);
-    } else {
+            k_walk_coherent<W, false><<<g, kThreads, 0, st>>>(a);
+    };
+    switch (traversal) {
+    case 1: coherent(std::integral_constant<int, 32>{}); break;
+    case 2: coherent(std::integral_constant<int, 16>{}); break;
+    case 3: coherent(std::integral_constant<int, 64>{}); break;
+    default:
         if (count)
             k_walk_independent<true><<<grid, kThreads, 0, st>>>(a);
         else
