@@ -92,6 +92,8 @@ WORKLOADS = {
     "plummer_4096": dict(kind="plummer", n=4096, seed=PAGES_SEED, theta=0.5),
     "plummer_16384": dict(kind="plummer", n=16384, seed=PAGES_SEED, theta=0.5),
     "plummer_131072": dict(kind="plummer", n=131072, seed=PAGES_SEED, theta=0.5),
+    "plummer_262144": dict(kind="plummer", n=262144, seed=PAGES_SEED, theta=0.5),
+    "plummer_524288": dict(kind="plummer", n=524288, seed=PAGES_SEED, theta=0.5),
     "plummer_1048576": dict(kind="plummer", n=1048576, seed=PAGES_SEED, theta=0.5),
     "two_spheres_2x1048576": dict(kind="two_spheres", n=2 * 1048576, seed=(1, 2), theta=0.5),
 }

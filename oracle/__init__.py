@@ -103,6 +103,8 @@ def _bind(lib):
     lib.oracle_quantise.restype = ctypes.c_uint32
     lib.oracle_rsqrt_rn.argtypes = [f32]
     lib.oracle_rsqrt_rn.restype = f32
+    lib.oracle_rsqrt_newton.argtypes = [f32]
+    lib.oracle_rsqrt_newton.restype = f32
     lib.oracle_interleave.argtypes = [ctypes.c_uint32] * 3
     lib.oracle_interleave.restype = ctypes.c_uint64
     lib.oracle_keys.argtypes = [P, i64, P, f32, P]
@@ -168,6 +170,11 @@ def quantise(x: float, lo: float, inv: float) -> int:
 def rsqrt_rn(x: float) -> np.float32:
     """The binary32 value nearest 1/sqrt(x) (the force term's inverse root)."""
     return np.float32(_load().oracle_rsqrt_rn(float(np.float32(x))))
+
+
+def rsqrt_newton(x: float) -> np.float32:
+    """The force term's inverse square root (fixed seed + three Newton steps)."""
+    return np.float32(_load().oracle_rsqrt_newton(float(np.float32(x))))
 
 
 def interleave(qx: int, qy: int, qz: int) -> int:

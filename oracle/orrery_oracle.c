@@ -24,9 +24,9 @@
  *
  * Precision. The pages measure single precision. Every floating-point step
  * below is one binary32 operation rounded to nearest-even: +, -, *, /, fmaf
- * (one rounding), and the inverse square root of the force term, which is
- * the binary32 value nearest 1/sqrt(x) (oracle_rsqrt_rn). The file is
- * compiled with -ffp-contract=off so the compiler adds no fused operations.
+ * (one rounding); the force term's inverse square root is itself a fixed
+ * sequence of such operations (oracle_rsqrt_newton). The file is compiled
+ * with -ffp-contract=off so the compiler adds no fused operations.
  * Where the pages leave the arithmetic open, the reading taken is written at
  * the step; the same readings are listed in the design notes.
  *
@@ -298,7 +298,7 @@ int oracle_moments(const float *ps, const int32_t *nodes, int64_t num_nodes, int
 /*                                                                          */
 /* Term for a source (x_j, m_j), Plummer softening, G = 1:                  */
 /*   r2 = fl(d2 + eps2), eps2 = fl(eps * eps)                               */
-/*   y  = rsqrt_rn(r2), the binary32 value nearest 1/sqrt(r2)               */
+/*   y  = oracle_rsqrt_newton(r2), 1/sqrt(r2) within 2 ulp (see there)      */
 /*   f  = fl(fl(m_j * y) * fl(y * y))       (m_j r2^(-3/2))                 */
 /*   a_ia = fmaf(f, dx_a, a_ia), in walk order                              */
 /* Cell terms use (M, CoM) with the d2 of the acceptance test.              */
@@ -347,6 +347,26 @@ float oracle_rsqrt_rn(float x)
     return y;
 }
 
+/* 1/sqrt(x) by a fixed binary32 recipe: the bit-level seed of C. Lomont,
+ * "Fast Inverse Square Root" (2003), i.e. the integer 0x5f375a86 minus half
+ * the bits of x, followed by three Newton-Raphson steps for 1/sqrt,
+ * y <- y * (3/2 - (x/2) y^2), each evaluated as fl(y * fma(-h, fl(y*y), 1.5))
+ * with h = fl(0.5 * x). For normal x (x >= 2^-126) the result is within
+ * 2 ulp of 1/sqrt(x) (the seed is good to 3.5 %, each step squares the
+ * error). Zero, subnormal and infinite x follow the same recipe and give no
+ * meaningful value; r2 >= eps^2 keeps x normal whenever eps >= 1.1e-19. */
+float oracle_rsqrt_newton(float x)
+{
+    uint32_t bits;
+    memcpy(&bits, &x, sizeof bits);
+    bits = 0x5f375a86u - (bits >> 1);
+    float y;
+    memcpy(&y, &bits, sizeof y);
+    const float h = 0.5f * x;
+    for (int it = 0; it < 3; ++it) y = y * fmaf(-h, y * y, 1.5f);
+    return y;
+}
+
 static void add_term(const float xi[3], float xj, float yj, float zj, float m, float eps2,
                      float acc[3])
 {
@@ -355,7 +375,7 @@ static void add_term(const float xi[3], float xj, float yj, float zj, float m, f
     float dz = zj - xi[2];
     float d2 = fmaf(dz, dz, fmaf(dy, dy, dx * dx));
     float r2 = d2 + eps2;
-    float y = oracle_rsqrt_rn(r2);
+    float y = oracle_rsqrt_newton(r2);
     float f = (m * y) * (y * y);
     acc[0] = fmaf(f, dx, acc[0]);
     acc[1] = fmaf(f, dy, acc[1]);

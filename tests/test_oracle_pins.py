@@ -189,6 +189,27 @@ def test_rsqrt_is_correctly_rounded():
     pin_rsqrt_rn()
 
 
+def pin_rsqrt_newton():
+    """The force term's inverse root is within 2 ulp of 1/sqrt(x) over the
+    normal binary32 range (checked against the correctly rounded value, which
+    pin_rsqrt_rn pins to rational arithmetic)."""
+    rng = np.random.default_rng(12)
+    xs = np.concatenate([rng.uniform(0.0025, 100.0, 20000),
+                         10.0 ** rng.uniform(-37.9, 38.3, 20000),
+                         np.float32(2.0) ** np.arange(-126, 128)]).astype(np.float32)
+    worst = 0
+    for x in xs:
+        y = oracle.rsqrt_newton(x)
+        c = oracle.rsqrt_rn(x)
+        ulps = abs(int(np.float32(y).view(np.int32)) - int(np.float32(c).view(np.int32)))
+        worst = max(worst, ulps)
+    assert worst <= 2
+
+
+def test_rsqrt_newton_within_two_ulp():
+    pin_rsqrt_newton()
+
+
 def test_quantise_floor_and_clamp():
     inv = np.float32(2 ** 21)  # side 1
     assert oracle.quantise(0.0, 0.0, inv) == 0
@@ -555,6 +576,8 @@ MISTAKES = [
      "return cell_side_sq(side, level) <= theta2 * d2;", pin_degenerate),
     ("last lane dropped from the union", "i < (g + 1) * width && i < n",
      "i < (g + 1) * width - 1 && i < n", pin_group_union),
+    ("two Newton steps instead of three", "for (int it = 0; it < 3; ++it) y = y * fmaf",
+     "for (int it = 0; it < 2; ++it) y = y * fmaf", pin_rsqrt_newton),
     ("inverse root midpoint test reversed", "if (fma(mid * mid, xd, -1.0) < 0.0) return up;",
      "if (fma(mid * mid, xd, -1.0) > 0.0) return up;", pin_rsqrt_rn),
     ("inverse root as 1/sqrtf without correction",

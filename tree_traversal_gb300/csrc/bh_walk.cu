@@ -15,13 +15,14 @@
 //   accept iff (side 2^-L)^2 < theta^2 |CoM_k - x_i|^2  -> cell term, escape
 //   else if k is a leaf -> particle terms over its particles j != i, escape
 //   else -> k + 1 (first child)
-// Term: r2 = d2 + eps^2, y = the binary32 value nearest 1/sqrt(r2),
-// f = (m y)(y y), a += f (x_src - x_i) by fused multiply-add. Every
-// floating-point step is one correctly rounded binary32 operation (explicit
-// _rn intrinsics), so decisions and sums do not depend on contraction choices.
+// Term: r2 = d2 + eps^2, y = rsqrt_newton(r2), f = (m y)(y y), a += f
+// (x_src - x_i) by fused multiply-add. Every floating-point step is one
+// correctly rounded binary32 operation (explicit _rn intrinsics), so
+// decisions and sums do not depend on contraction choices, and a CPU
+// restatement of the same steps reproduces them bit for bit.
 //
-// GB300 shape of the coherent kernel: the node k is warp-uniform, so its two
-// 16-byte records are read once per warp step and broadcast. The walk record
+// GB300 shape of the coherent kernel: the node k is group-uniform, so its two
+// 16-byte records are read once per group step and broadcast. The walk record
 // {escape, first, leaf count (0 = internal), squared side bits} carries
 // everything a step decides on, so a step needs no table lookup and no leaf
 // test beyond one compare. An opened leaf's particles are staged into shared
@@ -59,11 +60,25 @@ struct WalkArgs {
     uint32_t *cnt_s;
 };
 
+// 1/sqrt(x) by a fixed binary32 recipe: the bit-level seed of C. Lomont,
+// "Fast Inverse Square Root" (2003) -- the integer 0x5f375a86 minus half the
+// bits of x -- then three Newton-Raphson steps y <- y (3/2 - (x/2) y^2), each
+// as fl(y * fma(-h, fl(y y), 3/2)) with h = fl(x/2). Within 2 ulp of 1/sqrt(x)
+// for normal x; no MUFU and no branch, and reproducible on any IEEE CPU.
+__device__ __forceinline__ float rsqrt_newton(float x)
+{
+    const float h = __fmul_rn(0.5f, x);
+    float y = __int_as_float(0x5f375a86 - (int)((unsigned)__float_as_int(x) >> 1));
+#pragma unroll
+    for (int it = 0; it < 3; ++it) y = __fmul_rn(y, __fmaf_rn(-h, __fmul_rn(y, y), 1.5f));
+    return y;
+}
+
 __device__ __forceinline__ void add_term(float dx, float dy, float dz, float d2, float m,
                                          float eps2, float &ax, float &ay, float &az)
 {
     const float r2 = __fadd_rn(d2, eps2);
-    const float y = __frsqrt_rn(r2);
+    const float y = rsqrt_newton(r2);
     const float f = __fmul_rn(__fmul_rn(m, y), __fmul_rn(y, y));
     ax = __fmaf_rn(f, dx, ax);
     ay = __fmaf_rn(f, dy, ay);
@@ -95,7 +110,7 @@ __device__ __forceinline__ bool prologue(const WalkArgs &a, int &num_nodes, bool
         s_state[1] = P->num_nodes;
         bool ok = a.eps2 > 0.0f;
         if (ok) {
-            const float y = __frsqrt_rn(a.eps2);
+            const float y = rsqrt_newton(a.eps2);
             const float f = __fmul_rn(__fmul_rn(P->mmax, y), __fmul_rn(y, y));
             ok = isfinite(f);
         }
@@ -109,30 +124,15 @@ __device__ __forceinline__ bool prologue(const WalkArgs &a, int &num_nodes, bool
 
 // One coherence group = W consecutive sorted targets sharing one node index.
 // W = 16: half a warp per group (two groups per warp, each advancing on its
-// own, as the pages' sub-group width of 16); W = 32: one warp; W = 64: one
+// own, like the pages' sub-group width of 16); W = 32: one warp; W = 64: one
 // warp with two targets per lane (the width the pages could not measure).
-// Lanes hold targets base + i*G + lane for i < T, where G = lanes per group
-// and T = targets per lane.
+// Lane l of a group holds targets base + i*G + l for i < T, with G lanes per
+// group and T targets per lane.
 template <int W>
 struct Group {
     static constexpr int G = W < 32 ? W : 32;
     static constexpr int T = W > 32 ? W / 32 : 1;
 };
-
-// Cell or particle term with a per-target predicate: a target that does not
-// take the term gets f = 0, and fma(0, d, a) = a exactly (d is finite and a
-// is never -0), so masking by selection leaves its sum bit-identical.
-__device__ __forceinline__ void masked_term(bool take, float dx, float dy, float dz, float d2,
-                                            float m, float eps2, float &ax, float &ay, float &az)
-{
-    const float r2 = __fadd_rn(d2, eps2);
-    const float y = __frsqrt_rn(r2);
-    float f = __fmul_rn(__fmul_rn(m, y), __fmul_rn(y, y));
-    f = take ? f : 0.0f;
-    ax = __fmaf_rn(f, dx, ax);
-    ay = __fmaf_rn(f, dy, ay);
-    az = __fmaf_rn(f, dz, az);
-}
 
 template <int W, bool kCount, bool kSelfFree>
 __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, float4 *stage)
@@ -142,8 +142,7 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
     const int lane = threadIdx.x & 31;
     const int glane = lane & (G - 1);
     const unsigned gmask = (G == 32) ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
-    const int gid = (blockIdx.x * kThreads + threadIdx.x) / G;  // group index
-    const int base = gid * W;
+    const int base = ((blockIdx.x * kThreads + threadIdx.x) / G) * W;
 
     int tgt[T], next[T];
     bool valid[T];
@@ -159,50 +158,35 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
         ax[i] = ay[i] = az[i] = 0.0f;
         pc[i] = pp[i] = 0;
     }
-    auto group_min = [&]() {
+    int steps = 0;
+    for (; steps <= num_nodes; ++steps) {
         int v = next[0];
 #pragma unroll
         for (int i = 1; i < T; ++i) v = min(v, next[i]);
-        return __reduce_min_sync(gmask, v);
-    };
-    int k = group_min();
-    float4 c = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    int4 w = make_int4(0, 0, 0, 0);
-    if (k < num_nodes) {
-        c = __ldg(a.com + k);
-        w = __ldg(a.wnode + k);
-    }
-    int steps = 0;
-    for (; k < num_nodes && steps <= num_nodes; ++steps) {
-        // the next node is k + 1 whenever any lane descends (and after every
-        // leaf): start its loads now, ahead of this step's arithmetic
-        const int kp = min(k + 1, num_nodes - 1);
-        const float4 cp = __ldg(a.com + kp);
-        const int4 wp = __ldg(a.wnode + kp);
-
-        const float side2 = __int_as_float(w.w);
-        const bool leaf = w.z != 0;
-        bool acc[T], open[T];
-        float dx[T], dy[T], dz[T], d2[T];
-        bool any_acc = false, any_open = false;
+        const int k = __reduce_min_sync(gmask, v);
+        if (k >= num_nodes) break;
+        const float4 c = __ldg(a.com + k);
+        const int4 w = __ldg(a.wnode + k);
+        bool open[T];
+        bool any_open = false;
 #pragma unroll
         for (int i = 0; i < T; ++i) {
-            const bool act = next[i] == k;
-            dx[i] = __fsub_rn(c.x, xi[i].x);
-            dy[i] = __fsub_rn(c.y, xi[i].y);
-            dz[i] = __fsub_rn(c.z, xi[i].z);
-            d2[i] = dist2(dx[i], dy[i], dz[i]);
-            acc[i] = act && side2 < __fmul_rn(a.theta2, d2[i]);
-            open[i] = act && !acc[i] && leaf;
-            next[i] = act ? ((acc[i] || leaf) ? w.x : k + 1) : next[i];
-            if (kCount) pc[i] += acc[i] ? 1u : 0u;
-            any_acc |= acc[i];
+            open[i] = false;
+            if (next[i] == k) {
+                const float dx = __fsub_rn(c.x, xi[i].x);
+                const float dy = __fsub_rn(c.y, xi[i].y);
+                const float dz = __fsub_rn(c.z, xi[i].z);
+                const float d2 = dist2(dx, dy, dz);
+                if (__int_as_float(w.w) < __fmul_rn(a.theta2, d2)) {
+                    add_term(dx, dy, dz, d2, c.w, a.eps2, ax[i], ay[i], az[i]);
+                    if (kCount) ++pc[i];
+                    next[i] = w.x;
+                } else {
+                    open[i] = w.z != 0;
+                    next[i] = open[i] ? w.x : k + 1;
+                }
+            }
             any_open |= open[i];
-        }
-        if (__any_sync(gmask, any_acc)) {
-#pragma unroll
-            for (int i = 0; i < T; ++i)
-                masked_term(acc[i], dx[i], dy[i], dz[i], d2[i], c.w, a.eps2, ax[i], ay[i], az[i]);
         }
         if (__any_sync(gmask, any_open)) {
             const int first = w.y, count = w.z;
@@ -210,43 +194,32 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
                 if (glane == 0) atomicOr(&a.P->status, kStatusInternal);
                 break;
             }
-            if (kCount) {
 #pragma unroll
-                for (int i = 0; i < T; ++i)
-                    pp[i] += open[i] ? count - ((unsigned)(tgt[i] - first) < (unsigned)count ? 1u : 0u)
-                                     : 0u;
-            }
+            for (int i = 0; i < T; ++i)
+                if (kCount && open[i])
+                    pp[i] += count - ((unsigned)(tgt[i] - first) < (unsigned)count ? 1u : 0u);
             for (int b = 0; b < count; b += G) {
                 const int chunk = min(G, count - b);
                 if (glane < chunk) stage[glane] = __ldg(a.ps + first + b + glane);
                 __syncwarp(gmask);
-#pragma unroll 2
-                for (int j = 0; j < chunk; ++j) {
-                    const float4 p = stage[j];
 #pragma unroll
-                    for (int i = 0; i < T; ++i) {
-                        const bool take = kSelfFree ? open[i] : (open[i] && first + b + j != tgt[i]);
-                        const float ex = __fsub_rn(p.x, xi[i].x);
-                        const float ey = __fsub_rn(p.y, xi[i].y);
-                        const float ez = __fsub_rn(p.z, xi[i].z);
-                        masked_term(take, ex, ey, ez, dist2(ex, ey, ez), p.w, a.eps2, ax[i], ay[i],
-                                    az[i]);
+                for (int i = 0; i < T; ++i) {
+                    if (!open[i]) continue;
+                    if (kSelfFree) {
+#pragma unroll 4
+                        for (int j = 0; j < chunk; ++j)
+                            particle_term(stage[j], xi[i], a.eps2, ax[i], ay[i], az[i]);
+                    } else {
+                        const int self = tgt[i] - (first + b);
+                        for (int j = 0; j < chunk; ++j)
+                            if (j != self) particle_term(stage[j], xi[i], a.eps2, ax[i], ay[i], az[i]);
                     }
                 }
                 __syncwarp(gmask);
             }
         }
-        const int k2 = group_min();
-        if (k2 == k + 1) {
-            c = cp;
-            w = wp;
-        } else if (k2 < num_nodes) {
-            c = __ldg(a.com + k2);
-            w = __ldg(a.wnode + k2);
-        }
-        k = k2;
     }
-    if (k < num_nodes && glane == 0) atomicOr(&a.P->status, kStatusWalkBound);
+    if (steps > num_nodes && glane == 0) atomicOr(&a.P->status, kStatusWalkBound);
 #pragma unroll
     for (int i = 0; i < T; ++i) {
         if (!valid[i]) continue;
@@ -269,9 +242,8 @@ __global__ void __launch_bounds__(kThreads) k_walk_coherent(WalkArgs a)
     int num_nodes;
     bool self_free;
     if (!prologue(a, num_nodes, self_free)) return;  // block-uniform
-    const int lane = threadIdx.x & 31;
     constexpr int G = Group<W>::G;
-    float4 *stage = &s_leaf[threadIdx.x >> 5][lane & ~(G - 1)];
+    float4 *stage = &s_leaf[threadIdx.x >> 5][(threadIdx.x & 31) & ~(G - 1)];
     if (self_free)
         coherent_walk<W, kCount, true>(a, num_nodes, stage);
     else
