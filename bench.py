@@ -50,7 +50,50 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=8.0,
                    help="target wall time of the CPU-oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--crossover", action="store_true",
+                   help="instead of the benchmark line, time the tree against direct "
+                        "summation over a range of N (one JSON line per N)")
     return p.parse_args()
+
+
+def run_crossover(args) -> None:
+    """Tree (whole evaluation) against direct summation, Plummer spheres of
+    1024 .. 262144 particles: the pages' "Against the two solvers it has to
+    beat" table, on this GPU. Median of --steps timed calls after --warmup."""
+    import torch
+
+    import tree_traversal_gb300 as tt
+    from inputs import plummer
+    from tree_traversal_gb300.build import build
+
+    build()
+    tt.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        ms = []
+        for it in range(args.warmup + args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            if it >= args.warmup:
+                ms.append(a.elapsed_time(b))
+        return statistics.median(ms)
+
+    for n in (1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072, 262144):
+        pos_np, mass_np = plummer(n)
+        pos = torch.from_numpy(pos_np).to(dev)
+        mass = torch.from_numpy(mass_np).to(dev)
+        t_tree = timed(lambda: tt.bh_forces(pos, mass, 0.5, 0.05, 32, args.traversal))
+        walk = tt.last_timings()["walk_ms"]
+        t_direct = timed(lambda: tt.direct_forces(pos, mass, 0.05))
+        print(json.dumps({"n": n, "tree_ms": t_tree, "tree_walk_ms": walk, "direct_ms": t_direct,
+                          "tree_speedup_vs_direct": t_direct / t_tree,
+                          "direct_pairs_per_s": n * (n - 1) / (t_direct / 1000.0),
+                          "traversal": args.traversal}), flush=True)
 
 
 def measured_peaks() -> dict:
@@ -200,6 +243,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.crossover:
+        run_crossover(args)
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

@@ -172,6 +172,17 @@ int orrery_bh_tree(const float *pos_d, const float *mass_d, int64_t n, int32_t l
                    float *cube_d, uint64_t *keys_d, uint32_t *perm_d, int32_t *nodes_d,
                    float *com_d, int64_t max_nodes, int64_t *num_nodes, void *stream);
 
+/*
+ * Direct summation over every pair, the solver the pages time the tree
+ * against (docs/performance/sycl_tree.md, "Against the two solvers it has to
+ * beat"): acc_i = sum over j != i, j ascending in caller order, of the tree's
+ * particle term (same softening and arithmetic, no approximation). O(n^2).
+ *   pos_d [n][3], mass_d [n], acc_d [n][3]: device float32, caller order.
+ * Returns ORRERY_OK, ORRERY_EINVAL, ORRERY_ENONFINITE or ORRERY_ECUDA.
+ */
+int orrery_direct_forces(const float *pos_d, const float *mass_d, int64_t n, float eps,
+                         float *acc_d, void *stream);
+
 /* Upper bound of the node count for n particles and a leaf capacity:
  * n + 21 * floor(n / (leaf_cap + 1)) + 1 (leaves are disjoint and non-empty;
  * internal cells of one level are disjoint and hold more than leaf_cap).

@@ -127,6 +127,8 @@ def _bind(lib):
     lib.oracle_bh_forces.restype = i64
     lib.oracle_direct_f64.argtypes = [P, P, i64, f64, P, i64, P, ctypes.c_int]
     lib.oracle_direct_f64.restype = ctypes.c_int
+    lib.oracle_direct_f32.argtypes = [P, P, i64, f32, P, i64, P, ctypes.c_int]
+    lib.oracle_direct_f32.restype = ctypes.c_int
     lib.oracle_bh_recursive.argtypes = [P, P, i64, i32, f32, f32, f32, P, P]
     lib.oracle_bh_recursive.restype = ctypes.c_int
     return lib
@@ -355,6 +357,24 @@ def direct_f64(pos, mass, eps: float = 0.05, targets=None, threads: int | None =
                                    _ptr(out), int(threads or default_threads()))
     if rc != 0:
         raise RuntimeError("oracle_direct_f64")
+    return out
+
+
+def direct_f32(pos, mass, eps: float = 0.05, targets=None, threads: int | None = None) -> np.ndarray:
+    """Direct sum in binary32 with the walk's particle term, j ascending in
+    caller order; targets are original indices. [t,3] float32."""
+    pos = _f32(pos).reshape(-1, 3)
+    mass = _f32(mass).reshape(-1)
+    if targets is None:
+        nt, tp = pos.shape[0], None
+    else:
+        tgt = np.ascontiguousarray(targets, dtype=np.int64)
+        nt, tp = tgt.shape[0], _ptr(tgt)
+    out = np.zeros((nt, 3), np.float32)
+    rc = _load().oracle_direct_f32(_ptr(pos), _ptr(mass), pos.shape[0], float(eps), tp, nt,
+                                   _ptr(out), int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle_direct_f32")
     return out
 
 

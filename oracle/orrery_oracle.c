@@ -687,6 +687,65 @@ int oracle_direct_f64(const float *pos, const float *mass, int64_t n, double eps
 }
 
 /* ------------------------------------------------------------------------ */
+/* Direct summation in binary32 with the walk's own particle term, j        */
+/* ascending in caller order, j != i: the GPU direct kernel's definition    */
+/* (the pages' Phase 9 solver, [PERF] "Against the two solvers it has to    */
+/* beat"). targets: original indices (NULL = 0..n_targets-1).               */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    const float *pos, *mass;
+    int64_t n;
+    float eps2;
+    const int64_t *targets;
+    int64_t begin, end;
+    float *acc;
+} direct32_slice;
+
+static void *direct32_worker(void *arg)
+{
+    direct32_slice *d = (direct32_slice *)arg;
+    for (int64_t q = d->begin; q < d->end; ++q) {
+        int64_t i = d->targets ? d->targets[q] : q;
+        const float xi[3] = {d->pos[3 * i], d->pos[3 * i + 1], d->pos[3 * i + 2]};
+        float a[3] = {0.0f, 0.0f, 0.0f};
+        for (int64_t j = 0; j < d->n; ++j) {
+            if (j == i) continue;
+            add_term(xi, d->pos[3 * j], d->pos[3 * j + 1], d->pos[3 * j + 2], d->mass[j], d->eps2, a);
+        }
+        for (int c = 0; c < 3; ++c) d->acc[3 * q + c] = a[c];
+    }
+    return NULL;
+}
+
+int oracle_direct_f32(const float *pos, const float *mass, int64_t n, float eps,
+                      const int64_t *targets, int64_t n_targets, float *acc, int threads)
+{
+    if (threads < 1) threads = 1;
+    if (threads > 256) threads = 256;
+    if (n_targets < threads) threads = (int)(n_targets > 0 ? n_targets : 1);
+    pthread_t tid[256];
+    direct32_slice sl[256];
+    for (int w = 0; w < threads; ++w) {
+        sl[w].pos = pos;
+        sl[w].mass = mass;
+        sl[w].n = n;
+        sl[w].eps2 = eps * eps;
+        sl[w].targets = targets;
+        sl[w].begin = n_targets * w / threads;
+        sl[w].end = n_targets * (w + 1) / threads;
+        sl[w].acc = acc;
+    }
+    if (threads == 1) {
+        direct32_worker(&sl[0]);
+        return 0;
+    }
+    for (int w = 0; w < threads; ++w)
+        if (pthread_create(&tid[w], NULL, direct32_worker, &sl[w]) != 0) return -1;
+    for (int w = 0; w < threads; ++w) pthread_join(tid[w], NULL);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Cross-check 2: a pointer octree built and walked recursively.            */
 /* Built on its own from the sorted keys (an explicit child array per cell, */
 /* no escape indices), moments by recursion, and a recursive walk that       */

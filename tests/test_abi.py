@@ -38,6 +38,7 @@ def declared_functions() -> list[str]:
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("orrery_bh_forces", "orrery_bh_forces_host", "orrery_bh_tree",
+                 "orrery_direct_forces",
                  "orrery_bh_max_nodes", "orrery_bh_last_timings", "orrery_bh_kernel_launches",
                  "orrery_bh_strerror", "orrery_bh_release"):
         assert want in names
@@ -79,6 +80,11 @@ def test_argument_checks_answer_on_the_host(lib):
     assert f(dummy, dummy, 10, 0.5, 0.05, 32, 1, P, P, P, P) == L.EINVAL
     # node bound beyond int32: 2^30 particles with leaf capacity 1
     assert f(dummy, dummy, 1 << 30, 0.5, 0.05, 1, 1, dummy, P, P, P) == L.ERANGE
+    d = lib.orrery_direct_forces
+    assert d(dummy, dummy, -1, 0.05, dummy, P) == L.EINVAL
+    assert d(dummy, dummy, 10, float("nan"), dummy, P) == L.EINVAL
+    assert d(P, dummy, 10, 0.05, dummy, P) == L.EINVAL
+    assert d(P, P, 0, 0.05, P, P) == L.OK
     # n == 0 launches nothing and succeeds, whatever the pointers
     assert f(P, P, 0, 0.5, 0.05, 32, 0, P, P, P, P) == L.OK
     assert lib.orrery_bh_forces_host(P, P, 0, 0.5, 0.05, 32, 1, P, P, P, P) == L.OK

@@ -309,3 +309,27 @@ def test_full_size_plummer_1m(tt):
 def test_full_size_two_spheres_theta_sweep(tt):
     pos, mass = two_spheres(1048576)
     check_full_size(tt, pos, mass, [0.3, 0.5, 0.7])
+
+
+# ---------------------------------------------------------------------------
+# direct summation (the pages' comparison solver)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [1, 2, 33, 255, 256, 257, 1000, 4097, 20000])
+def test_direct_bit_exact(tt, n):
+    pos, mass = plummer(n, 1000 + n)
+    acc = tt.direct_forces(dev(pos), dev(mass), EPS)
+    ref = oracle.direct_f32(pos, mass, EPS)
+    assert np.array_equal(acc.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_direct_coincident_and_nonfinite(tt):
+    pos, mass, cap, T = case("duplicates_65")
+    acc = tt.direct_forces(dev(pos), dev(mass), EPS)
+    assert np.array_equal(acc.cpu().numpy().view(np.uint32),
+                          oracle.direct_f32(pos, mass, EPS).view(np.uint32))
+    p = pos.copy()
+    p[3, 0] = np.inf
+    with pytest.raises(tt.OrreryError) as e:
+        tt.direct_forces(dev(p), dev(mass), EPS)
+    assert e.value.status == -2
+    assert tt.direct_forces(torch.zeros((0, 3), device="cuda"), torch.zeros(0, device="cuda")).shape == (0, 3)

@@ -388,6 +388,26 @@ def test_theta0_is_direct_sum():
     pin_theta0_is_direct()
 
 
+def pin_direct_f32():
+    # against the compensated fp64 sum (binary32 rounding only) ...
+    pos, m = plummer(3000, 41)
+    got = oracle.direct_f32(pos, m, EPS)
+    assert oracle.relative_error(got, oracle.direct_f64(pos, m, EPS)).max() < 2e-5
+    # ... and, on input already in Morton order with one leaf holding every
+    # particle, equal bit for bit to the theta = 0 tree walk (same pairs, same order)
+    pos, m = plummer(700, 42)
+    perm, _ = oracle.sort(oracle.keys(pos))
+    ps, ms = pos[perm], m[perm]
+    acc, inter, _, _, _ = oracle.bh_forces(ps, ms, 0.0, EPS, 1000)
+    assert np.array_equal(oracle.direct_f32(ps, ms, EPS).view(np.uint32), acc.view(np.uint32))
+    tg = np.array([3, 0, 699])
+    assert np.array_equal(oracle.direct_f32(ps, ms, EPS, tg), oracle.direct_f32(ps, ms, EPS)[tg])
+
+
+def test_direct_f32():
+    pin_direct_f32()
+
+
 def test_direct_f64_against_numpy():
     pos, m = uniform_cube(200, 8)
     ref = direct_numpy(pos, m, EPS)

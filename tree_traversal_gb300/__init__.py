@@ -14,6 +14,7 @@ from .bh import (  # noqa: F401
     bh_forces,
     bh_forces_host,
     bh_tree,
+    direct_forces,
     kernel_launches,
     last_timings,
     max_nodes,

@@ -83,6 +83,8 @@ def load(path: str | None = None):
         lib.orrery_bh_forces_host.restype = ctypes.c_int
         lib.orrery_bh_forces_noalloc.argtypes = [P, P, i64, f32, f32, i32, i32, P, P, P, P]
         lib.orrery_bh_forces_noalloc.restype = ctypes.c_int
+        lib.orrery_direct_forces.argtypes = [P, P, i64, f32, P, P]
+        lib.orrery_direct_forces.restype = ctypes.c_int
         lib.orrery_bh_tree.argtypes = [P, P, i64, i32, P, P, P, P, P, i64,
                                        ctypes.POINTER(ctypes.c_int64), P]
         lib.orrery_bh_tree.restype = ctypes.c_int

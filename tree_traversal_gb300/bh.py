@@ -107,6 +107,23 @@ def bh_forces_host(pos: np.ndarray, mass: np.ndarray, theta: float = 0.5, eps: f
     return acc, inter, visits
 
 
+def direct_forces(pos: torch.Tensor, mass: torch.Tensor, eps: float = 0.05, out=None):
+    """Direct O(n^2) summation of the same softened law (every pair, caller
+    order), on the current CUDA stream. Returns acc [n, 3] float32."""
+    n = int(pos.shape[0]) if pos.dim() == 2 else -1
+    _check_device(pos, "pos", (n, 3))
+    _check_device(mass, "mass", (n,))
+    dev = pos.device
+    acc = torch.empty((n, 3), dtype=torch.float32, device=dev) if out is None else out
+    _check_device(acc, "acc", (n, 3))
+    with torch.cuda.device(dev):
+        rc = _lib.load().orrery_direct_forces(_ptr(pos), _ptr(mass), n, float(eps), _ptr(acc),
+                                              _stream_handle(dev))
+    if rc != _lib.OK:
+        raise _lib.OrreryError(rc, "orrery_direct_forces")
+    return acc
+
+
 def max_nodes(n: int, leaf_cap: int = 32) -> int:
     v = _lib.load().orrery_bh_max_nodes(int(n), int(leaf_cap))
     if v < 0:

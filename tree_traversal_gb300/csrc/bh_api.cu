@@ -379,6 +379,25 @@ int orrery_bh_tree(const float *pos_d, const float *mass_d, int64_t n, int32_t l
     return nn > max_nodes ? ORRERY_ERANGE : ORRERY_OK;
 }
 
+int orrery_direct_forces(const float *pos_d, const float *mass_d, int64_t n, float eps,
+                         float *acc_d, void *stream)
+{
+    if (n < 0 || n > kMaxN || !(eps >= 0.0f)) return ORRERY_EINVAL;
+    if (n == 0) return ORRERY_OK;
+    if (!pos_d || !mass_d || !acc_d) return ORRERY_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace *w = nullptr;
+    int rc = get_workspace(1, node_bound(1, 1), &w);  // only the status word is used
+    if (rc != ORRERY_OK) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaMemsetAsync(&w->b.params->status, 0, sizeof(int), st);
+    launch_direct(pos_d, mass_d, n, eps, acc_d, &w->b.params->status, st);
+    cudaMemcpyAsync(w->host_params, w->b.params, sizeof(DeviceParams), cudaMemcpyDeviceToHost, st);
+    if (cudaStreamSynchronize(st) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+        return ORRERY_ECUDA;
+    return (w->host_params->status & kStatusNonFinite) ? ORRERY_ENONFINITE : ORRERY_OK;
+}
+
 int64_t orrery_bh_max_nodes(int64_t n, int32_t leaf_cap)
 {
     if (n < 0 || n > kMaxN || leaf_cap < 1) return -1;

@@ -83,6 +83,8 @@ void launch_walk(int traversal, float theta, float eps, int32_t leaf_cap, bool c
                  const Buffers &b, cudaStream_t st);
 void launch_scatter(const uint32_t *perm, const Buffers &b, float *acc, uint32_t *inter,
                     uint32_t *visits, cudaStream_t st);
+void launch_direct(const float *pos, const float *mass, int64_t n, float eps, float *acc,
+                   int *status, cudaStream_t st);
 void launch_scan_u32(const uint32_t *in, uint32_t *out, int64_t count, uint32_t *partial,
                      cudaStream_t st);
 void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *partial,
