@@ -45,7 +45,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--workload", default="plummer_1048576")
     p.add_argument("--traversal", default="coherent",
-                   choices=["coherent", "coherent16", "coherent64", "independent"])
+                   choices=["coherent", "coherent16", "coherent64", "ballot", "together",
+                            "independent"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=8.0,
                    help="target wall time of the CPU-oracle sample")

@@ -62,15 +62,22 @@ extern "C" {
                                   its fixed scratch array */
 
 /* Which traversal the walk kernel runs ("sycl_tree_solver.hpp",
- * TreeTraversal). All compute the same function of the input; the coherent
- * ones differ only in how many consecutive sorted targets share one node
- * index (the coherence width; docs/performance/sycl_tree.md, "The sub-group
- * width"), which changes the visit counts they report and their speed. */
+ * TreeTraversal). Values 0-3 and 5 compute the same function of the input; the
+ * coherent ones differ only in how many consecutive sorted targets share one
+ * node index (the coherence width; docs/performance/sycl_tree.md, "The
+ * sub-group width"), which changes the visit counts they report and their
+ * speed. Value 4 is the published scheme the pages reject (ADR-0029,
+ * Alternatives considered): a warp descends wherever any of its 32 targets
+ * must, and accepts a cell only when all do, so a target's sum depends on
+ * its warp-mates. It is kept to measure that contrast, not for use. */
 typedef enum {
-    ORRERY_INDEPENDENT = 0,  /* one thread per target, each on its own node index */
-    ORRERY_COHERENT = 1,     /* 32 targets (one warp) share a node index */
-    ORRERY_COHERENT_16 = 2,  /* 16 targets (half a warp) share a node index */
-    ORRERY_COHERENT_64 = 3   /* 64 targets (one warp, two per lane) share a node index */
+    ORRERY_INDEPENDENT = 0,       /* one thread per target, each on its own node index */
+    ORRERY_COHERENT = 1,          /* 32 targets (one warp) share a node index */
+    ORRERY_COHERENT_16 = 2,       /* 16 targets (half a warp) share a node index */
+    ORRERY_COHERENT_64 = 3,       /* 64 targets (one warp, two per lane) share a node index */
+    ORRERY_DESCEND_TOGETHER = 4,  /* comparison only: group-dependent answer */
+    ORRERY_COHERENT_BALLOT = 5    /* as ORRERY_COHERENT, next node by vote + escape
+                                     instead of a minimum reduction (same visits) */
 } orrery_traversal;
 
 /* Where the last evaluation spent its time ("sycl_tree_solver.hpp",

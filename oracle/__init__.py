@@ -123,6 +123,9 @@ def _bind(lib):
     lib.oracle_group_visits.argtypes = [P, P, P, i64, i32, f32, f32, f32, i64, i32, P,
                                         i64, P]
     lib.oracle_group_visits.restype = ctypes.c_int
+    lib.oracle_descend_together.argtypes = [P, P, P, i64, i32, f32, f32, f32, i64, i32, P, P,
+                                            P, P]
+    lib.oracle_descend_together.restype = ctypes.c_int
     lib.oracle_bh_forces.argtypes = [P, P, i64, f32, f32, i32, P, P, P, P, ctypes.c_int]
     lib.oracle_bh_forces.restype = i64
     lib.oracle_direct_f64.argtypes = [P, P, i64, f64, P, i64, P, ctypes.c_int]
@@ -307,6 +310,16 @@ class Tree:
         if rc != 0:
             raise MemoryError("oracle_group_visits")
         return out
+
+    def descend_together(self, theta: float, eps: float, width: int = 32):
+        """The rejected group-descending scheme (sorted order): (acc, pc, pp, visits)."""
+        acc = np.zeros((self.n, 3), np.float32)
+        pc = np.zeros(self.n, np.uint32)
+        pp = np.zeros(self.n, np.uint32)
+        vis = np.zeros(self.n, np.uint32)
+        _load().oracle_descend_together(*self._args(theta, eps), self.n, int(width), _ptr(acc),
+                                        _ptr(pc), _ptr(pp), _ptr(vis))
+        return acc, pc, pp, vis
 
     def recursive(self, theta: float, eps: float):
         """Cross-check: pointer tree + recursive walk, sorted order.

@@ -524,6 +524,68 @@ int oracle_group_visits(const float *ps, const int32_t *nodes, const float *cm, 
 }
 
 /* ------------------------------------------------------------------------ */
+/* The rejected alternative, for comparison ([ADR29] Alternatives considered,*/
+/* "Descend wherever any lane must, and let the accepting lanes descend      */
+/* too"). A group of `width` consecutive sorted targets walks one node       */
+/* index. At node k every target of the group takes the criterion; if all   */
+/* accept, each adds the cell term and the group jumps to escape(k); else   */
+/* if k is a leaf, each adds the terms of all the leaf's particles but its   */
+/* own and the group jumps to escape(k); else the group descends to k + 1,  */
+/* the would-be acceptors with it. Each target's sum now depends on which   */
+/* targets share its group. Counters are per target as in the walk; visits */
+/* are the group's steps. Outputs in sorted order.                           */
+/* ------------------------------------------------------------------------ */
+int oracle_descend_together(const float *ps, const int32_t *nodes, const float *cm,
+                            int64_t num_nodes, int32_t leaf_cap, float side, float theta,
+                            float eps, int64_t n, int32_t width, float *acc, uint32_t *pc,
+                            uint32_t *pp, uint32_t *visits)
+{
+    const float theta2 = theta * theta;
+    const float eps2 = eps * eps;
+    for (int64_t g = 0; g * width < n; ++g) {
+        const int64_t lo = g * width;
+        const int64_t hi = (lo + width < n) ? lo + width : n;
+        for (int64_t i = lo; i < hi; ++i) {
+            acc[3 * i] = acc[3 * i + 1] = acc[3 * i + 2] = 0.0f;
+            pc[i] = pp[i] = visits[i] = 0;
+        }
+        int64_t k = 0;
+        while (k < num_nodes) {
+            const int32_t *node = nodes + 4 * k;
+            const float *c = cm + 4 * k;
+            int all_accept = 1;
+            for (int64_t i = lo; i < hi; ++i) {
+                const float xi[3] = {ps[4 * i], ps[4 * i + 1], ps[4 * i + 2]};
+                visits[i] += 1;
+                if (!accept_cell(xi, c, side, node[3], theta2)) all_accept = 0;
+            }
+            if (all_accept) {
+                for (int64_t i = lo; i < hi; ++i) {
+                    const float xi[3] = {ps[4 * i], ps[4 * i + 1], ps[4 * i + 2]};
+                    add_term(xi, c[0], c[1], c[2], c[3], eps2, acc + 3 * i);
+                    pc[i] += 1;
+                }
+                k = node[0];
+            } else if (node_is_leaf(node, leaf_cap)) {
+                for (int64_t i = lo; i < hi; ++i) {
+                    const float xi[3] = {ps[4 * i], ps[4 * i + 1], ps[4 * i + 2]};
+                    for (int64_t j = node[1]; j < (int64_t)node[1] + node[2]; ++j) {
+                        if (j == i) continue;
+                        add_term(xi, ps[4 * j], ps[4 * j + 1], ps[4 * j + 2], ps[4 * j + 3], eps2,
+                                 acc + 3 * i);
+                        pp[i] += 1;
+                    }
+                }
+                k = node[0];
+            } else {
+                k = k + 1;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Step 10: one whole force evaluation, outputs in the caller's order.      */
 /* Gathers the particles into tree order and scatters the results back      */
 /* ([SOLVER] "Where the tree comes from").                                  */

@@ -25,8 +25,8 @@ from inputs import PAGES_SEED, plummer, two_spheres, uniform_cube
 pytestmark = pytest.mark.gpu
 EPS = 0.05
 REL_TOL = 1e-5
-WIDTH = {"coherent": 32, "coherent16": 16, "coherent64": 64}
-TRAVERSALS = ["coherent", "independent", "coherent16", "coherent64"]
+WIDTH = {"coherent": 32, "coherent16": 16, "coherent64": 64, "ballot": 32}
+TRAVERSALS = ["coherent", "independent", "coherent16", "coherent64", "ballot"]
 
 
 @pytest.fixture(scope="module")
@@ -333,3 +333,20 @@ def test_direct_coincident_and_nonfinite(tt):
         tt.direct_forces(dev(p), dev(mass), EPS)
     assert e.value.status == -2
     assert tt.direct_forces(torch.zeros((0, 3), device="cuda"), torch.zeros(0, device="cuda")).shape == (0, 3)
+
+
+# ---------------------------------------------------------------------------
+# the rejected descend-together scheme, against its own oracle
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["plummer_4096", "ragged_5003_cap7", "duplicates_65", "grid_ties_cap4",
+                                  "tiny_33_cap1", "two_spheres_2x8192"])
+def test_descend_together_bit_exact(tt, name):
+    pos, mass, cap, T = case(name)
+    for theta in (0.5, 0.0, 0.8):
+        acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), theta, EPS, cap, "together")
+        r_acc, r_pc, r_pp, r_vis = T.descend_together(theta, EPS, 32)
+        g = acc.cpu().numpy()[T.perm]
+        assert np.array_equal(g.view(np.uint32), r_acc.view(np.uint32))
+        gi = u32(inter)[T.perm]
+        assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)
+        assert np.array_equal(u32(vis)[T.perm], r_vis)

@@ -570,6 +570,24 @@ def test_coherent_soft_pins():
     assert np.all(T.group_visits(0.0, EPS) == T.num_nodes)
 
 
+def test_descend_together_contrast():
+    # ADR-0029, Alternatives considered: descending with the group visits the
+    # same nodes (the union), performs more interactions, and is more accurate;
+    # at width 1 it is the independent walk itself
+    pos, m = plummer(4096)
+    T = oracle.Tree(pos, m, 32)
+    a, pc, pp, v = T.walk(0.5, EPS)
+    a1, pc1, pp1, v1 = T.descend_together(0.5, EPS, 1)
+    assert np.array_equal(a1.view(np.uint32), a.view(np.uint32))
+    assert np.array_equal(pc1, pc) and np.array_equal(pp1, pp) and np.array_equal(v1, v)
+    ad, pcd, ppd, vd = T.descend_together(0.5, EPS, 32)
+    assert np.array_equal(vd, np.repeat(T.group_visits(0.5, EPS, 32), 32)[: T.n])
+    assert (pcd + ppd).sum() > 1.3 * (pc + pp).sum()
+    ref = oracle.direct_f64(pos, m, EPS)[T.perm]
+    rms = lambda e: math.sqrt((e ** 2).mean())
+    assert rms(oracle.relative_error(ad, ref)) < 0.7 * rms(oracle.relative_error(a, ref))
+
+
 def test_two_spheres_generator_layout():
     pos, m = two_spheres(1000)
     assert pos.shape == (2000, 3) and np.all(m == np.float32(1 / 1000))

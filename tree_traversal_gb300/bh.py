@@ -14,7 +14,8 @@ import torch
 from . import _lib
 
 _TRAVERSALS = {"independent": _lib.INDEPENDENT, "coherent": _lib.COHERENT,
-               "coherent16": _lib.COHERENT_16, "coherent64": _lib.COHERENT_64}
+               "coherent16": _lib.COHERENT_16, "coherent64": _lib.COHERENT_64,
+               "together": _lib.DESCEND_TOGETHER, "ballot": _lib.COHERENT_BALLOT}
 _TRAVERSALS.update({v: v for v in list(_TRAVERSALS.values())})
 
 

@@ -134,7 +134,16 @@ struct Group {
     static constexpr int T = W > 32 ? W / 32 : 1;
 };
 
-template <int W, bool kCount, bool kSelfFree>
+// kBallot selects how the group finds its next node. The default takes the
+// minimum over the lanes' wanted indices (ADR-0029, Decision). The ballot form
+// (ADR-0029, Alternatives considered: "Vote on whether to descend, and
+// otherwise follow the current node's escape index") goes to k + 1 if any
+// lane active at k descends and to escape(k) otherwise. With per-lane skip
+// indices both pick the same node -- a lane inactive at k waits at the escape
+// of an accepted ancestor of k, which is never below escape(k) -- so the
+// ballot form visits exactly the same union; it is kept to measure the cost
+// of the two instructions against each other.
+template <int W, bool kCount, bool kSelfFree, bool kBallot = false>
 __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, float4 *stage)
 {
     constexpr int G = Group<W>::G;
@@ -159,16 +168,23 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
         pc[i] = pp[i] = 0;
     }
     int steps = 0;
+    int kb = __any_sync(gmask, valid[0]) ? 0 : num_nodes;  // the ballot form's node
     for (; steps <= num_nodes; ++steps) {
-        int v = next[0];
+        int k;
+        if (kBallot) {
+            k = kb;
+        } else {
+            int v = next[0];
 #pragma unroll
-        for (int i = 1; i < T; ++i) v = min(v, next[i]);
-        const int k = __reduce_min_sync(gmask, v);
+            for (int i = 1; i < T; ++i) v = min(v, next[i]);
+            k = __reduce_min_sync(gmask, v);
+        }
         if (k >= num_nodes) break;
         const float4 c = __ldg(a.com + k);
         const int4 w = __ldg(a.wnode + k);
         bool open[T];
         bool any_open = false;
+        bool descend = false;
 #pragma unroll
         for (int i = 0; i < T; ++i) {
             open[i] = false;
@@ -184,10 +200,12 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
                 } else {
                     open[i] = w.z != 0;
                     next[i] = open[i] ? w.x : k + 1;
+                    descend |= !open[i];
                 }
             }
             any_open |= open[i];
         }
+        if (kBallot) kb = __any_sync(gmask, descend) ? k + 1 : w.x;
         if (__any_sync(gmask, any_open)) {
             const int first = w.y, count = w.z;
             if (first < 0 || first > a.n - count) {  // group-uniform consistency check
@@ -235,7 +253,7 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
     }
 }
 
-template <int W, bool kCount>
+template <int W, bool kCount, bool kBallot = false>
 __global__ void __launch_bounds__(kThreads) k_walk_coherent(WalkArgs a)
 {
     __shared__ float4 s_leaf[kWarpsPerBlock][32];
@@ -245,9 +263,97 @@ __global__ void __launch_bounds__(kThreads) k_walk_coherent(WalkArgs a)
     constexpr int G = Group<W>::G;
     float4 *stage = &s_leaf[threadIdx.x >> 5][(threadIdx.x & 31) & ~(G - 1)];
     if (self_free)
-        coherent_walk<W, kCount, true>(a, num_nodes, stage);
+        coherent_walk<W, kCount, true, kBallot>(a, num_nodes, stage);
     else
-        coherent_walk<W, kCount, false>(a, num_nodes, stage);
+        coherent_walk<W, kCount, false, kBallot>(a, num_nodes, stage);
+}
+
+// The scheme the pages reject, kept as a measured contrast (ADR-0029,
+// Alternatives considered: "Descend wherever any lane must, and let the
+// accepting lanes descend too"). One node index per warp; at node k the warp
+// accepts only if every target accepts (each then adds the cell term),
+// otherwise a leaf is opened for every target and an internal node is
+// entered by all. Each target's sum depends on which targets share its warp,
+// so this is a different function of the input from the walks above.
+template <bool kCount, bool kSelfFree>
+__device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, float4 *stage)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kThreads + threadIdx.x;
+    const bool valid = t < a.n;
+    const float4 xi = valid ? __ldg(a.ps + t) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float ax = 0.0f, ay = 0.0f, az = 0.0f;
+    uint32_t pc = 0, pp = 0;
+    int k = 0, steps = 0;
+    for (; k < num_nodes && steps <= num_nodes; ++steps) {
+        const float4 c = __ldg(a.com + k);
+        const int4 w = __ldg(a.wnode + k);
+        const float dx = __fsub_rn(c.x, xi.x);
+        const float dy = __fsub_rn(c.y, xi.y);
+        const float dz = __fsub_rn(c.z, xi.z);
+        const float d2 = dist2(dx, dy, dz);
+        const bool accept = __int_as_float(w.w) < __fmul_rn(a.theta2, d2);
+        if (__all_sync(0xffffffffu, accept || !valid)) {
+            if (valid) {
+                add_term(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
+                if (kCount) ++pc;
+            }
+            k = w.x;
+        } else if (w.z != 0) {
+            const int first = w.y, count = w.z;
+            if (first < 0 || first > a.n - count) {  // warp-uniform consistency check
+                if (lane == 0) atomicOr(&a.P->status, kStatusInternal);
+                break;
+            }
+            if (kCount && valid)
+                pp += count - ((unsigned)(t - first) < (unsigned)count ? 1u : 0u);
+            for (int b = 0; b < count; b += 32) {
+                const int chunk = min(32, count - b);
+                if (lane < chunk) stage[lane] = __ldg(a.ps + first + b + lane);
+                __syncwarp();
+                if (valid) {
+                    if (kSelfFree) {
+#pragma unroll 4
+                        for (int j = 0; j < chunk; ++j)
+                            particle_term(stage[j], xi, a.eps2, ax, ay, az);
+                    } else {
+                        const int self = t - (first + b);
+                        for (int j = 0; j < chunk; ++j)
+                            if (j != self) particle_term(stage[j], xi, a.eps2, ax, ay, az);
+                    }
+                }
+                __syncwarp();
+            }
+            k = w.x;
+        } else {
+            k = k + 1;
+        }
+    }
+    if (k < num_nodes && lane == 0) atomicOr(&a.P->status, kStatusWalkBound);
+    if (valid) {
+        a.acc_s[3 * (int64_t)t + 0] = ax;
+        a.acc_s[3 * (int64_t)t + 1] = ay;
+        a.acc_s[3 * (int64_t)t + 2] = az;
+        if (kCount) {
+            a.cnt_s[3 * (int64_t)t + 0] = pc;
+            a.cnt_s[3 * (int64_t)t + 1] = pp;
+            a.cnt_s[3 * (int64_t)t + 2] = (uint32_t)steps;
+        }
+    }
+}
+
+template <bool kCount>
+__global__ void __launch_bounds__(kThreads) k_walk_together(WalkArgs a)
+{
+    __shared__ float4 s_leaf[kWarpsPerBlock][32];
+    int num_nodes;
+    bool self_free;
+    if (!prologue(a, num_nodes, self_free)) return;  // block-uniform
+    float4 *stage = s_leaf[threadIdx.x >> 5];
+    if (self_free)
+        together_walk<kCount, true>(a, num_nodes, stage);
+    else
+        together_walk<kCount, false>(a, num_nodes, stage);
 }
 
 template <bool kCount, bool kSelfFree>
@@ -337,6 +443,18 @@ void launch_walk(int traversal, float theta, float eps, int32_t leaf_cap, bool c
     case 1: coherent(std::integral_constant<int, 32>{}); break;
     case 2: coherent(std::integral_constant<int, 16>{}); break;
     case 3: coherent(std::integral_constant<int, 64>{}); break;
+    case 4:
+        if (count)
+            k_walk_together<true><<<grid, kThreads, 0, st>>>(a);
+        else
+            k_walk_together<false><<<grid, kThreads, 0, st>>>(a);
+        break;
+    case 5:
+        if (count)
+            k_walk_coherent<32, true, true><<<grid, kThreads, 0, st>>>(a);
+        else
+            k_walk_coherent<32, false, true><<<grid, kThreads, 0, st>>>(a);
+        break;
     default:
         if (count)
             k_walk_independent<true><<<grid, kThreads, 0, st>>>(a);
