@@ -57,6 +57,23 @@ def parse():
     return p.parse_args()
 
 
+def replica_throughput(local_ms: float, local_units: float, steps: int, dist=None, device=None):
+    """Whole-job throughput of independent replicas: the slowest rank's time
+    (max over ranks) over the units every rank processed. Returns
+    (ms per step, units per second)."""
+    total_ms, units = float(local_ms), float(local_units)
+    if dist is not None and dist.is_initialized():
+        import torch
+
+        t = torch.tensor([total_ms, units], dtype=torch.float64, device=device)
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        total_ms, units = float(mx[0].item()), float(t[1].item())
+    ms_per_step = total_ms / steps
+    return ms_per_step, units / (ms_per_step / 1000.0)
+
+
 def run_crossover(args) -> None:
     """Tree (whole evaluation) against direct summation, Plummer spheres of
     1024 .. 262144 particles: the pages' "Against the two solvers it has to
@@ -316,13 +333,7 @@ def main():
         wall = time.perf_counter() - t0
     launches = tt.kernel_launches() - launches0
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    value = world * interactions / (ms_per_step / 1000.0)
+    ms_per_step, value = replica_throughput(sum(step_ms), interactions, args.steps, dist, device)
 
     def mean(key):
         return statistics.fmean(p[key] for p in phases)
