@@ -146,7 +146,7 @@ int orrery_bh_forces_host(const float *pos, const float *mass, int64_t n, float 
  * is one fixed 16 MiB array inside the library's device code, which every GPU
  * that loads the library holds until the process exits. A call fits iff its
  * buffers fit 16 MiB: at leaf_cap >= 16 every n <= 65536 fits; at leaf_cap 32
- * up to 83968 particles fit. A call that does not fit returns ORRERY_ESCRATCH
+ * every n <= 80000 fits. A call that does not fit returns ORRERY_ESCRATCH
  * before launching anything.
  *
  * The first call on each device looks up the array's device address (with

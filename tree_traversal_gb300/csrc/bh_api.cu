@@ -91,8 +91,8 @@ size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
     b.keys_b = (uint64_t *)take(sizeof(uint64_t) * (size_t)n);
     b.idx_a = (uint32_t *)take(sizeof(uint32_t) * (size_t)n);
     b.idx_b = (uint32_t *)take(sizeof(uint32_t) * (size_t)n);
-    b.radix_hist = (uint32_t *)take(sizeof(uint32_t) * 256 * (size_t)b.radix_blocks);
-    b.radix_total = (uint32_t *)take(sizeof(uint32_t) * 256);
+    b.radix_hist = (uint32_t *)take(sizeof(uint32_t) * radix_bins() * (size_t)b.radix_blocks);
+    b.radix_total = (uint32_t *)take(sizeof(uint32_t) * radix_bins());
     b.ps = (float4 *)take(sizeof(float4) * (size_t)n);
     b.lev_d = (int8_t *)take(n1);
     b.lev_w = (int8_t *)take(n1);

@@ -42,8 +42,8 @@ struct Buffers {
     // a2, a3
     uint64_t *keys_a, *keys_b;
     uint32_t *idx_a, *idx_b;
-    uint32_t *radix_hist;     // [256][radix_blocks], digit-major
-    uint32_t *radix_total;    // [256]
+    uint32_t *radix_hist;     // [bins][radix_blocks], digit-major
+    uint32_t *radix_total;    // [bins]
     // a4
     float4 *ps;               // sorted {x, y, z, m}
     // a5
@@ -91,6 +91,7 @@ void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *p
                     cudaStream_t st);
 int64_t scan_partial_count(int64_t count);
 int radix_blocks_for(int64_t n);
+int radix_bins();
 
 // --- small device helpers -------------------------------------------------
 // Number of leading 3-bit groups (levels) two 63-bit keys share: 0..21.
