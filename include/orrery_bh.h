@@ -90,8 +90,9 @@ typedef struct {
     float gather_ms;  /* particles into tree order */
     float build_ms;   /* octree nodes and escape indices */
     float moments_ms; /* upward mass / centre-of-mass pass */
-    float walk_ms;    /* the traversal */
-    float scatter_ms; /* results back to caller order */
+    float walk_ms;    /* the traversal, which also writes the results back to
+                         the caller's order (the scatter is fused into it) */
+    float scatter_ms; /* 0: fused into walk_ms */
     float d2h_ms;     /* orrery_bh_forces_host only: device-to-host copies */
     float total_ms;   /* first event to last */
     int32_t traversal;

@@ -107,8 +107,6 @@ size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
     b.sums = (float4 *)take(sizeof(float4) * (size_t)nodes);
     b.com = (float4 *)take(sizeof(float4) * (size_t)nodes);
     b.wnode = (int4 *)take(sizeof(int4) * (size_t)nodes);
-    b.acc_s = (float *)take(sizeof(float) * 3 * (size_t)n);
-    b.cnt_s = (uint32_t *)take(sizeof(uint32_t) * 3 * (size_t)n);
     return off;
 }
 
@@ -238,10 +236,9 @@ int forces_device(Workspace &w, const float *pos, const float *mass, int64_t n, 
     uint64_t *keys_sorted = nullptr;
     uint32_t *perm = nullptr;
     run_tree(w, pos, mass, cap, st, &keys_sorted, &perm);
-    launch_walk(traversal, theta, eps, cap, inter != nullptr || visits != nullptr, w.b, st);
+    launch_walk(traversal, theta, eps, perm, w.b, acc, inter, visits, st);
     cudaEventRecord(w.ev[EV_WALK], st);
-    launch_scatter(perm, w.b, acc, inter, visits, st);
-    cudaEventRecord(w.ev[EV_SCATTER], st);
+    cudaEventRecord(w.ev[EV_SCATTER], st);  // the scatter is fused into the walk
     if (host) {
         cudaMemcpyAsync(host->acc, acc, 12 * (size_t)n, cudaMemcpyDeviceToHost, st);
         if (host->inter)

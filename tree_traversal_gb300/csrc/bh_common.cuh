@@ -62,9 +62,6 @@ struct Buffers {
     float4 *com;              // [max_nodes] {CoM_x, CoM_y, CoM_z, M}
     int4 *wnode;              // [max_nodes] walk record {escape, first, leaf count or 0,
                               //  bits of the node's squared side}
-    // a7
-    float *acc_s;             // [n][3] sorted order
-    uint32_t *cnt_s;          // [n][3] {pc, pp, visits} sorted order
 };
 
 // Kernel-launch counter (every launch site increments it).
@@ -79,10 +76,9 @@ void launch_gather(const float *pos, const float *mass, const uint32_t *perm, co
 void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b,
                   cudaStream_t st);
 void launch_moments(int32_t leaf_cap, const Buffers &b, cudaStream_t st);
-void launch_walk(int traversal, float theta, float eps, int32_t leaf_cap, bool count,
-                 const Buffers &b, cudaStream_t st);
-void launch_scatter(const uint32_t *perm, const Buffers &b, float *acc, uint32_t *inter,
-                    uint32_t *visits, cudaStream_t st);
+// a7 with the a8 scatter fused: results land in the caller's order
+void launch_walk(int traversal, float theta, float eps, const uint32_t *perm, const Buffers &b,
+                 float *acc, uint32_t *inter, uint32_t *visits, cudaStream_t st);
 void launch_direct(const float *pos, const float *mass, int64_t n, float eps, float *acc,
                    int *status, cudaStream_t st);
 void launch_scan_u32(const uint32_t *in, uint32_t *out, int64_t count, uint32_t *partial,

@@ -83,8 +83,6 @@ size_t layout(Buffers &b, char *base, int64_t n, int64_t nodes)
     b.sums = (float4 *)take(16 * (size_t)nodes);
     b.com = (float4 *)take(16 * (size_t)nodes);
     b.wnode = (int4 *)take(16 * (size_t)nodes);
-    b.acc_s = (float *)take(12 * (size_t)n);
-    b.cnt_s = (uint32_t *)take(12 * (size_t)n);
     return off;
 }
 
@@ -141,9 +139,7 @@ extern "C" int orrery_bh_forces_noalloc(const float *pos_d, const float *mass_d,
     launch_gather(pos_d, mass_d, perm, b, st);
     launch_build(keys_sorted, leaf_cap, b, st);
     launch_moments(leaf_cap, b, st);
-    launch_walk(traversal, theta, eps, leaf_cap, interactions_d != nullptr || visits_d != nullptr,
-                b, st);
-    launch_scatter(perm, b, acc_d, interactions_d, visits_d, st);
+    launch_walk(traversal, theta, eps, perm, b, acc_d, interactions_d, visits_d, st);
     int status = 0;
     cudaMemcpyAsync(&status, &b.params->status, sizeof(int), cudaMemcpyDeviceToHost, st);
     if (cudaStreamSynchronize(st) != cudaSuccess || cudaGetLastError() != cudaSuccess)

@@ -1,6 +1,7 @@
-// bh_prep.cu -- the data-movement phases around the tree: bounding cube,
-// Morton keys, gather into tree order, scatter back, and a device-wide
-// exclusive scan used by the build.
+// bh_prep.cu -- the data-movement phases before the tree: bounding cube,
+// Morton keys, gather into tree order, and a device-wide exclusive scan used
+// by the build. (The scatter back to the caller's order is fused into the
+// walk's epilogue.)
 //
 // Pages: "sycl_tree_solver.hpp" (Detailed Description, "Where the tree comes
 // from": particles are copied into the tree's sorted order before the walk
@@ -187,29 +188,6 @@ k_gather(const float *__restrict__ pos, const float *__restrict__ mass,
                         __ldg(pos + 3 * (int64_t)i + 2), __ldg(mass + i));
 }
 
-// a8: results back to the caller's order.
-__global__ void __launch_bounds__(256)
-k_scatter(const uint32_t *__restrict__ perm, int64_t n, const float *__restrict__ acc_s,
-          const uint32_t *__restrict__ cnt_s, float *__restrict__ acc,
-          uint32_t *__restrict__ inter, uint32_t *__restrict__ visits, int *status)
-{
-    int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= n) return;
-    int64_t i = __ldg(perm + k);
-    if (i >= n) {
-        atomicOr(status, kStatusInternal);
-        return;
-    }
-    acc[3 * i + 0] = acc_s[3 * k + 0];
-    acc[3 * i + 1] = acc_s[3 * k + 1];
-    acc[3 * i + 2] = acc_s[3 * k + 2];
-    if (inter) {
-        inter[2 * i + 0] = cnt_s[3 * k + 0];
-        inter[2 * i + 1] = cnt_s[3 * k + 1];
-    }
-    if (visits) visits[i] = cnt_s[3 * k + 2];
-}
-
 // ---- exclusive scan of uint32 (three launches, no inter-block waiting) ----
 constexpr int kScanThreads = 256;
 constexpr int kScanItems = 8;
@@ -338,14 +316,6 @@ void launch_gather(const float *pos, const float *mass, const uint32_t *perm, co
                    cudaStream_t st)
 {
     k_gather<<<ceil_div(b.n, 256), 256, 0, st>>>(pos, mass, perm, b.n, b.ps, &b.params->status);
-    g_launches += 1;
-}
-
-void launch_scatter(const uint32_t *perm, const Buffers &b, float *acc, uint32_t *inter,
-                    uint32_t *visits, cudaStream_t st)
-{
-    k_scatter<<<ceil_div(b.n, 256), 256, 0, st>>>(perm, b.n, b.acc_s, b.cnt_s, acc, inter, visits,
-                                                   &b.params->status);
     g_launches += 1;
 }
 

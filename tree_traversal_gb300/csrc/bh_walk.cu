@@ -1,4 +1,5 @@
-// bh_walk.cu -- a7: the two stackless traversals of the depth-first octree.
+// bh_walk.cu -- a7 (with a8 fused): the stackless traversals of the depth-first
+// octree; each target writes its results to its caller-order slot.
 //
 // orrery: "sycl_tree_solver.hpp", TreeTraversal:
 //   kIndependent -- one thread per target, each following its own node index;
@@ -49,16 +50,40 @@ constexpr int kThreads = 256;
 constexpr int kWarpsPerBlock = kThreads / 32;
 
 struct WalkArgs {
-    const float4 *ps;     // sorted particles {x, y, z, m}
-    const float4 *com;    // {CoM_x, CoM_y, CoM_z, M}
-    const int4 *wnode;    // {escape, first, leaf count or 0, squared side bits}
+    const float4 *ps;      // sorted particles {x, y, z, m}
+    const float4 *com;     // {CoM_x, CoM_y, CoM_z, M}
+    const int4 *wnode;     // {escape, first, leaf count or 0, squared side bits}
+    const uint32_t *perm;  // caller index of each sorted slot
     int n;
     float theta2;
     float eps2;
     DeviceParams *P;
-    float *acc_s;
-    uint32_t *cnt_s;
+    float *acc;            // caller order [n][3]
+    uint32_t *inter;       // caller order [n][2] or null
+    uint32_t *visits;      // caller order [n] or null
 };
+
+// a8, fused: a target's results go straight to its caller-order slot.
+template <bool kCount>
+__device__ __forceinline__ void store_target(const WalkArgs &a, int t, float ax, float ay, float az,
+                                             uint32_t pc, uint32_t pp, uint32_t visits)
+{
+    const uint32_t o = __ldg(a.perm + t);
+    if (o >= (uint32_t)a.n) {
+        atomicOr(&a.P->status, kStatusInternal);
+        return;
+    }
+    a.acc[3 * (int64_t)o + 0] = ax;
+    a.acc[3 * (int64_t)o + 1] = ay;
+    a.acc[3 * (int64_t)o + 2] = az;
+    if (kCount) {
+        if (a.inter) {
+            a.inter[2 * (int64_t)o + 0] = pc;
+            a.inter[2 * (int64_t)o + 1] = pp;
+        }
+        if (a.visits) a.visits[o] = visits;
+    }
+}
 
 // 1/sqrt(x) by a fixed binary32 recipe: the bit-level seed of C. Lomont,
 // "Fast Inverse Square Root" (2003) -- the integer 0x5f375a86 minus half the
@@ -239,18 +264,8 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
     }
     if (steps > num_nodes && glane == 0) atomicOr(&a.P->status, kStatusWalkBound);
 #pragma unroll
-    for (int i = 0; i < T; ++i) {
-        if (!valid[i]) continue;
-        const int64_t t = tgt[i];
-        a.acc_s[3 * t + 0] = ax[i];
-        a.acc_s[3 * t + 1] = ay[i];
-        a.acc_s[3 * t + 2] = az[i];
-        if (kCount) {
-            a.cnt_s[3 * t + 0] = pc[i];
-            a.cnt_s[3 * t + 1] = pp[i];
-            a.cnt_s[3 * t + 2] = (uint32_t)steps;  // every step visits the group's union
-        }
-    }
+    for (int i = 0; i < T; ++i)  // every step visits the group's union
+        if (valid[i]) store_target<kCount>(a, tgt[i], ax[i], ay[i], az[i], pc[i], pp[i], steps);
 }
 
 template <int W, bool kCount, bool kBallot = false>
@@ -330,16 +345,7 @@ __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, 
         }
     }
     if (k < num_nodes && lane == 0) atomicOr(&a.P->status, kStatusWalkBound);
-    if (valid) {
-        a.acc_s[3 * (int64_t)t + 0] = ax;
-        a.acc_s[3 * (int64_t)t + 1] = ay;
-        a.acc_s[3 * (int64_t)t + 2] = az;
-        if (kCount) {
-            a.cnt_s[3 * (int64_t)t + 0] = pc;
-            a.cnt_s[3 * (int64_t)t + 1] = pp;
-            a.cnt_s[3 * (int64_t)t + 2] = (uint32_t)steps;
-        }
-    }
+    if (valid) store_target<kCount>(a, t, ax, ay, az, pc, pp, steps);
 }
 
 template <bool kCount>
@@ -391,14 +397,7 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
         }
     }
     if (k < num_nodes) atomicOr(&a.P->status, kStatusWalkBound);
-    a.acc_s[3 * (int64_t)t + 0] = ax;
-    a.acc_s[3 * (int64_t)t + 1] = ay;
-    a.acc_s[3 * (int64_t)t + 2] = az;
-    if (kCount) {
-        a.cnt_s[3 * (int64_t)t + 0] = pc;
-        a.cnt_s[3 * (int64_t)t + 1] = pp;
-        a.cnt_s[3 * (int64_t)t + 2] = (uint32_t)steps;
-    }
+    store_target<kCount>(a, t, ax, ay, az, pc, pp, steps);
 }
 
 template <bool kCount>
@@ -415,20 +414,22 @@ __global__ void __launch_bounds__(kThreads) k_walk_independent(WalkArgs a)
 
 }  // namespace
 
-void launch_walk(int traversal, float theta, float eps, int32_t leaf_cap, bool count,
-                 const Buffers &b, cudaStream_t st)
+void launch_walk(int traversal, float theta, float eps, const uint32_t *perm, const Buffers &b,
+                 float *acc, uint32_t *inter, uint32_t *visits, cudaStream_t st)
 {
-    (void)leaf_cap;  // leaf-ness is carried by the walk records
+    const bool count = inter != nullptr || visits != nullptr;
     WalkArgs a;
     a.ps = b.ps;
     a.com = b.com;
     a.wnode = b.wnode;
+    a.perm = perm;
     a.n = (int)b.n;
     a.theta2 = theta * theta;  // host binary32 products, round to nearest
     a.eps2 = eps * eps;
     a.P = b.params;
-    a.acc_s = b.acc_s;
-    a.cnt_s = b.cnt_s;
+    a.acc = acc;
+    a.inter = inter;
+    a.visits = visits;
     const unsigned grid = ceil_div(b.n, kThreads);
     // coherent groups of W targets: kThreads lanes cover kThreads * T targets
     auto coherent = [&](auto wtag) {
