@@ -90,6 +90,10 @@ CASES = {
     "unequal_masses_cap16": lambda: _masses(9000, 12),
     "uniform_20000_cap200": lambda: (*uniform_cube(20000, 6), 200),
     "two_spheres_2x8192": lambda: (*two_spheres(8192), 32),
+    # sizes on the radix tile (4096 keys) and scan tile (2048 entries) edges
+    "edge_2047": lambda: (*plummer(2047, 91), 32),
+    "edge_4095": lambda: (*plummer(4095, 92), 32),
+    "edge_8193_cap3": lambda: (*plummer(8193, 93), 3),
 }
 _cache = {}
 
@@ -227,6 +231,15 @@ def test_host_entry_point_matches_device(tt):
     assert t["h2d_ms"] >= 0 and t["d2h_ms"] >= 0 and t["total_ms"] >= t["walk_ms"]
     # pageable numpy buffers work too
     a2, i2, v2 = tt.bh_forces_host(pos, mass, 0.5, EPS, cap, "coherent")
+    assert np.array_equal(a2.view(np.uint32), acc.cpu().numpy().view(np.uint32))
+
+
+def test_host_entry_point_without_counters(tt):
+    pos, mass, cap, T = case("edge_4095")
+    acc, _, _ = tt.bh_forces(dev(pos), dev(mass), 0.5, EPS, cap, "coherent64")
+    out = (np.zeros((T.n, 3), np.float32), None, None)
+    a2, i2, v2 = tt.bh_forces_host(pos, mass, 0.5, EPS, cap, "coherent64", out=out)
+    assert i2 is None and v2 is None
     assert np.array_equal(a2.view(np.uint32), acc.cpu().numpy().view(np.uint32))
 
 

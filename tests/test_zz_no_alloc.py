@@ -66,6 +66,22 @@ def test_noalloc_matches_the_allocating_entry_point(lib):
             assert torch.equal(inter, inter0) and torch.equal(vis, vis0)
 
 
+def test_noalloc_every_traversal(lib):
+    import tree_traversal_gb300._lib as L
+    from inputs import plummer
+
+    pos_np, mass_np = plummer(9001, 17)
+    pos = torch.from_numpy(pos_np).cuda()
+    mass = torch.from_numpy(mass_np).cuda()
+    for trav in (L.INDEPENDENT, L.COHERENT, L.COHERENT_16, L.COHERENT_64, L.DESCEND_TOGETHER,
+                 L.COHERENT_BALLOT):
+        r0 = _call(lib.orrery_bh_forces, pos, mass, 0.5, 0.05, 32, trav)
+        r1 = _call(lib.orrery_bh_forces_noalloc, pos, mass, 0.5, 0.05, 32, trav)
+        assert r0[0] == r1[0] == L.OK
+        for a, b in zip(r0[1:], r1[1:]):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
 def test_noalloc_rejects_what_does_not_fit(lib):
     import tree_traversal_gb300._lib as L
 
