@@ -363,3 +363,39 @@ def test_descend_together_bit_exact(tt, name):
         gi = u32(inter)[T.perm]
         assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)
         assert np.array_equal(u32(vis)[T.perm], r_vis)
+
+
+# ---------------------------------------------------------------------------
+# repeated calls replay a captured graph: it must see new data in old buffers
+# ---------------------------------------------------------------------------
+def test_graph_replay_sees_new_inputs_and_survives_workspace_growth(tt):
+    pos, mass, cap, T = case("ragged_5003_cap7")
+    p, m = dev(pos), dev(mass)
+    acc = torch.empty((T.n, 3), device="cuda")
+    inter = torch.empty((T.n, 2), dtype=torch.int32, device="cuda")
+    vis = torch.empty(T.n, dtype=torch.int32, device="cuda")
+    out = (acc, inter, vis)
+    for _ in range(3):  # first call captures, the others replay
+        tt.bh_forces(p, m, 0.5, EPS, cap, "coherent", out=out)
+        check_tree_outputs(T, acc, inter, 0.5)
+        assert tt.last_timings()["launches"] > 0 and tt.last_timings()["walk_ms"] > 0
+    # new positions in the same buffers: the replayed graph reads them
+    pos2, mass2 = plummer(T.n, 555)
+    p.copy_(dev(pos2))
+    m.copy_(dev(mass2))
+    tt.bh_forces(p, m, 0.5, EPS, cap, "coherent", out=out)
+    check_tree_outputs(oracle.Tree(pos2, mass2, cap), acc, inter, 0.5)
+    # a larger call regrows the workspace (dropping every captured graph) ...
+    big = case("plummer_16384")
+    tt.bh_forces(dev(big[0]), dev(big[1]), 0.5, EPS, big[2], "coherent")
+    # ... and the small call still gives the exact answer afterwards
+    tt.bh_forces(p, m, 0.5, EPS, cap, "coherent", out=out)
+    check_tree_outputs(oracle.Tree(pos2, mass2, cap), acc, inter, 0.5)
+
+
+def check_tree_outputs(T, acc, inter, theta):
+    r_acc, r_pc, r_pp, _ = T.walk(theta, EPS)
+    g = acc.cpu().numpy()[T.perm]
+    assert np.array_equal(g.view(np.uint32), r_acc.view(np.uint32))
+    gi = u32(inter)[T.perm]
+    assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)

@@ -10,9 +10,11 @@
 // format directly, and the int32 bounds check it carried moves to the
 // argument checks below (node count bound against INT32_MAX).
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "../../include/orrery_bh.h"
 #include "bh_common.cuh"
@@ -38,6 +40,31 @@ enum Ev {
     EV_COUNT
 };
 
+// One replayable evaluation: every argument that the captured launches bake
+// in, plus the workspace base they point into.
+struct GraphKey {
+    const void *pos, *mass, *base;
+    void *acc, *inter, *visits;
+    int64_t n;
+    float theta, eps;
+    int32_t cap, traversal;
+    bool operator==(const GraphKey &o) const
+    {
+        return pos == o.pos && mass == o.mass && base == o.base && acc == o.acc &&
+               inter == o.inter && visits == o.visits && n == o.n && theta == o.theta &&
+               eps == o.eps && cap == o.cap && traversal == o.traversal;
+    }
+};
+
+struct GraphEntry {
+    GraphKey key;
+    cudaGraphExec_t exec;
+    uint64_t launches;  // kernels in the graph
+    uint64_t last_use;
+};
+
+constexpr size_t kGraphCache = 8;
+
 struct Workspace {
     int device = -1;
     void *base = nullptr;
@@ -50,7 +77,26 @@ struct Workspace {
     // device staging for orrery_bh_forces_host
     void *io = nullptr;
     int64_t io_n = -1;
+    // captured evaluations, replayed when a call repeats its arguments
+    cudaStream_t capture_stream = nullptr;
+    std::vector<GraphEntry> graphs;
+    uint64_t tick = 0;
 };
+
+void drop_graphs(Workspace *w)
+{
+    for (auto &g : w->graphs) cudaGraphExecDestroy(g.exec);
+    w->graphs.clear();
+}
+
+bool graphs_enabled()
+{
+    static const bool on = [] {
+        const char *v = getenv("ORRERY_GRAPHS");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
 
 std::mutex g_mu;
 Workspace *g_ws[kMaxDevices] = {};
@@ -116,6 +162,8 @@ void free_workspace(Workspace *w)
     int prev = -1;
     cudaGetDevice(&prev);
     cudaSetDevice(w->device);
+    drop_graphs(w);
+    if (w->capture_stream) cudaStreamDestroy(w->capture_stream);
     if (w->base) cudaFree(w->base);
     if (w->io) cudaFree(w->io);
     if (w->host_params) cudaFreeHost(w->host_params);
@@ -148,6 +196,7 @@ int get_workspace(int64_t n, int64_t nodes, Workspace **out)
     if (n > w->cap_n || nodes > w->cap_nodes) {
         const int64_t cn = n > w->cap_n ? n : w->cap_n;
         const int64_t cm = nodes > w->cap_nodes ? nodes : w->cap_nodes;
+        drop_graphs(w);  // they point into the old allocation
         if (w->base) cudaFree(w->base);
         w->base = nullptr;
         w->cap_n = w->cap_nodes = -1;
@@ -207,32 +256,27 @@ void run_tree(Workspace &w, const float *pos, const float *mass, int32_t cap, cu
     cudaEventRecord(w.ev[EV_MOMENTS], st);
 }
 
+int collect(Workspace &w, cudaStream_t st);
+
 int finish(Workspace &w, cudaStream_t st)
 {
     cudaMemcpyAsync(w.host_params, w.b.params, sizeof(DeviceParams), cudaMemcpyDeviceToHost, st);
-    if (cudaStreamSynchronize(st) != cudaSuccess || cudaGetLastError() != cudaSuccess)
-        return ORRERY_ECUDA;
-    const int s = w.host_params->status;
-    if (s & kStatusNonFinite) return ORRERY_ENONFINITE;
-    if (s & kStatusNodeBound) return ORRERY_ERANGE;
-    if (s & kStatusWalkBound) return ORRERY_EWALK;
-    if (s & kStatusInternal) return ORRERY_EINTERNAL;
-    return ORRERY_OK;
+    return collect(w, st);
 }
 
-// Enqueues phases a1..a8 and, for the host entry point, the result copies;
-// then blocks once and records the phase timings.
+// Host destinations of orrery_bh_forces_host.
 struct HostOut {
     float *acc;
     uint32_t *inter;
     uint32_t *visits;
 };
 
-int forces_device(Workspace &w, const float *pos, const float *mass, int64_t n, float theta,
-                  float eps, int32_t cap, int32_t traversal, float *acc, uint32_t *inter,
-                  uint32_t *visits, cudaStream_t st, const HostOut *host)
+// Enqueues phases a1..a8, for the host entry point the result copies, and
+// the read-back of the status word.
+void enqueue_forces(Workspace &w, const float *pos, const float *mass, int64_t n, float theta,
+                    float eps, int32_t cap, int32_t traversal, float *acc, uint32_t *inter,
+                    uint32_t *visits, cudaStream_t st, const HostOut *host)
 {
-    const uint64_t launches0 = g_launches.load();
     uint64_t *keys_sorted = nullptr;
     uint32_t *perm = nullptr;
     run_tree(w, pos, mass, cap, st, &keys_sorted, &perm);
@@ -247,7 +291,92 @@ int forces_device(Workspace &w, const float *pos, const float *mass, int64_t n, 
             cudaMemcpyAsync(host->visits, visits, 4 * (size_t)n, cudaMemcpyDeviceToHost, st);
         cudaEventRecord(w.ev[EV_D2H], st);
     }
-    const int rc = finish(w, st);
+    cudaMemcpyAsync(w.host_params, w.b.params, sizeof(DeviceParams), cudaMemcpyDeviceToHost, st);
+}
+
+// Blocks on the stream and turns the status word into a status code.
+int collect(Workspace &w, cudaStream_t st)
+{
+    if (cudaStreamSynchronize(st) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+        return ORRERY_ECUDA;
+    const int s = w.host_params->status;
+    if (s & kStatusNonFinite) return ORRERY_ENONFINITE;
+    if (s & kStatusNodeBound) return ORRERY_ERANGE;
+    if (s & kStatusWalkBound) return ORRERY_EWALK;
+    if (s & kStatusInternal) return ORRERY_EINTERNAL;
+    return ORRERY_OK;
+}
+
+// The cached graph of this call, captured on first use; nullptr when capture
+// is off or fails (the caller then launches directly). Capture runs on the
+// workspace's own stream, so it never touches the caller's stream.
+GraphEntry *graph_for(Workspace &w, const GraphKey &key, const float *pos, const float *mass,
+                      int64_t n, float theta, float eps, int32_t cap, int32_t traversal,
+                      float *acc, uint32_t *inter, uint32_t *visits)
+{
+    if (!graphs_enabled()) return nullptr;
+    for (auto &g : w.graphs)
+        if (g.key == key) {
+            g.last_use = ++w.tick;
+            return &g;
+        }
+    if (!w.capture_stream &&
+        cudaStreamCreateWithFlags(&w.capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        w.capture_stream = nullptr;
+        return nullptr;
+    }
+    prepare_sort();  // function attributes are set outside the capture
+    const uint64_t before = g_launches.load();
+    if (cudaStreamBeginCapture(w.capture_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    enqueue_forces(w, pos, mass, n, theta, eps, cap, traversal, acc, inter, visits,
+                   w.capture_stream, nullptr);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(w.capture_stream, &graph);
+    const uint64_t launches = g_launches.load() - before;
+    g_launches -= launches;  // captured, not launched
+    cudaGraphExec_t exec = nullptr;
+    const bool ok = ec == cudaSuccess && graph &&
+                    cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+    if (graph) cudaGraphDestroy(graph);
+    if (!ok) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (w.graphs.size() >= kGraphCache) {  // evict the least recently used
+        size_t old = 0;
+        for (size_t i = 1; i < w.graphs.size(); ++i)
+            if (w.graphs[i].last_use < w.graphs[old].last_use) old = i;
+        cudaGraphExecDestroy(w.graphs[old].exec);
+        w.graphs.erase(w.graphs.begin() + (long)old);
+    }
+    w.graphs.push_back(GraphEntry{key, exec, launches, ++w.tick});
+    return &w.graphs.back();
+}
+
+// Runs one evaluation: replays its captured graph when the call repeats the
+// arguments of an earlier one (device buffers only), else launches directly;
+// then blocks once and records the phase timings.
+int forces_device(Workspace &w, const float *pos, const float *mass, int64_t n, float theta,
+                  float eps, int32_t cap, int32_t traversal, float *acc, uint32_t *inter,
+                  uint32_t *visits, cudaStream_t st, const HostOut *host)
+{
+    const uint64_t launches0 = g_launches.load();
+    GraphEntry *g = nullptr;
+    if (!host) {
+        const GraphKey key{pos, mass, w.base, acc, inter, visits, n, theta, eps, cap, traversal};
+        g = graph_for(w, key, pos, mass, n, theta, eps, cap, traversal, acc, inter, visits);
+    }
+    if (g && cudaGraphLaunch(g->exec, st) == cudaSuccess) {
+        g_launches += g->launches;
+    } else {
+        if (g) cudaGetLastError();
+        enqueue_forces(w, pos, mass, n, theta, eps, cap, traversal, acc, inter, visits, st, host);
+    }
+    const int rc = collect(w, st);
     if (rc != ORRERY_OK) return rc;
     orrery_bh_timings t{};
     t.bbox_ms = ms_between(w.ev[EV_START], w.ev[EV_BBOX]);

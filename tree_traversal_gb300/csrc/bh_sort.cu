@@ -216,18 +216,23 @@ k_radix_scatter(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ v
 
 // Sorts b.keys_a (filled by the key phase) with the original indices as
 // values. Seven passes: the result lands in keys_b / idx_b.
-void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint32_t **perm)
+void prepare_sort()
 {
-    const int nb = b.radix_blocks;
-    const size_t smem = sizeof(ScatterSmem);
     static std::atomic<bool> configured[64];  // the opt-in is set once per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !configured[dev].load()) {
         cudaFuncSetAttribute(k_radix_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+                             (int)sizeof(ScatterSmem));
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
+}
+
+void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint32_t **perm)
+{
+    const int nb = b.radix_blocks;
+    const size_t smem = sizeof(ScatterSmem);
+    prepare_sort();
     uint64_t *kin = b.keys_a, *kout = b.keys_b;
     uint32_t *vin = b.idx_a, *vout = b.idx_b;
     for (int p = 0; p < kPasses; ++p) {
