@@ -226,6 +226,14 @@ int check_args(int64_t n, float theta, float eps, int32_t leaf_cap, int32_t trav
     return ORRERY_OK;
 }
 
+// Records a phase event. Under stream capture a plain record only orders
+// streams; the external flag makes it a node of the graph, so replays record
+// it as well.
+void record_event(cudaEvent_t ev, cudaStream_t st)
+{
+    cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+}
+
 float ms_between(cudaEvent_t a, cudaEvent_t b)
 {
     float ms = 0.0f;
@@ -241,19 +249,19 @@ void run_tree(Workspace &w, const float *pos, const float *mass, int32_t cap, cu
               uint64_t **keys_sorted, uint32_t **perm)
 {
     const Buffers &b = w.b;
-    cudaEventRecord(w.ev[EV_START], st);
+    record_event(w.ev[EV_START], st);
     launch_bbox(pos, mass, b, st);
-    cudaEventRecord(w.ev[EV_BBOX], st);
+    record_event(w.ev[EV_BBOX], st);
     launch_morton(pos, b, st);
-    cudaEventRecord(w.ev[EV_MORTON], st);
+    record_event(w.ev[EV_MORTON], st);
     launch_sort(b, st, keys_sorted, perm);
-    cudaEventRecord(w.ev[EV_SORT], st);
+    record_event(w.ev[EV_SORT], st);
     launch_gather(pos, mass, *perm, b, st);
-    cudaEventRecord(w.ev[EV_GATHER], st);
+    record_event(w.ev[EV_GATHER], st);
     launch_build(*keys_sorted, cap, b, st);
-    cudaEventRecord(w.ev[EV_BUILD], st);
+    record_event(w.ev[EV_BUILD], st);
     launch_moments(cap, b, st);
-    cudaEventRecord(w.ev[EV_MOMENTS], st);
+    record_event(w.ev[EV_MOMENTS], st);
 }
 
 int collect(Workspace &w, cudaStream_t st);
@@ -281,15 +289,15 @@ void enqueue_forces(Workspace &w, const float *pos, const float *mass, int64_t n
     uint32_t *perm = nullptr;
     run_tree(w, pos, mass, cap, st, &keys_sorted, &perm);
     launch_walk(traversal, theta, eps, perm, w.b, acc, inter, visits, st);
-    cudaEventRecord(w.ev[EV_WALK], st);
-    cudaEventRecord(w.ev[EV_SCATTER], st);  // the scatter is fused into the walk
+    record_event(w.ev[EV_WALK], st);
+    record_event(w.ev[EV_SCATTER], st);  // the scatter is fused into the walk
     if (host) {
         cudaMemcpyAsync(host->acc, acc, 12 * (size_t)n, cudaMemcpyDeviceToHost, st);
         if (host->inter)
             cudaMemcpyAsync(host->inter, inter, 8 * (size_t)n, cudaMemcpyDeviceToHost, st);
         if (host->visits)
             cudaMemcpyAsync(host->visits, visits, 4 * (size_t)n, cudaMemcpyDeviceToHost, st);
-        cudaEventRecord(w.ev[EV_D2H], st);
+        record_event(w.ev[EV_D2H], st);
     }
     cudaMemcpyAsync(w.host_params, w.b.params, sizeof(DeviceParams), cudaMemcpyDeviceToHost, st);
 }
@@ -462,7 +470,7 @@ int orrery_bh_forces_host(const float *pos, const float *mass, int64_t n, float 
     p += align256(8 * (size_t)w->io_n);
     uint32_t *vis_d = (uint32_t *)p;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaEventRecord(w->ev[EV_H2D0], st);
+    record_event(w->ev[EV_H2D0], st);
     cudaMemcpyAsync(pos_d, pos, 12 * (size_t)n, cudaMemcpyHostToDevice, st);
     cudaMemcpyAsync(mass_d, mass, 4 * (size_t)n, cudaMemcpyHostToDevice, st);
     const HostOut host{acc, interactions, visits};
