@@ -231,7 +231,12 @@ int check_args(int64_t n, float theta, float eps, int32_t leaf_cap, int32_t trav
 // it as well.
 void record_event(cudaEvent_t ev, cudaStream_t st)
 {
-    cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(st, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, st);
 }
 
 float ms_between(cudaEvent_t a, cudaEvent_t b)
