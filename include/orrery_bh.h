@@ -55,7 +55,9 @@ extern "C" {
 #define ORRERY_ERANGE (-3)     /* node count or size beyond the int32 range */
 #define ORRERY_ECUDA (-4)      /* a CUDA runtime call failed */
 #define ORRERY_EWALK (-5)      /* a walk exceeded its iteration bound */
-#define ORRERY_ENOMEM (-6)     /* the workspace could not be allocated */
+#define ORRERY_ENOMEM (-6)     /* the workspace could not be allocated (the environment
+                                  variable ORRERY_FAIL_ALLOC=1 forces this whenever the
+                                  workspace has to grow, to test callers' failure paths) */
 #define ORRERY_EINTERNAL (-7)  /* an index failed a device-side consistency check;
                                   the access was skipped (a library defect) */
 #define ORRERY_ESCRATCH (-8)   /* orrery_bh_forces_noalloc: the problem does not fit

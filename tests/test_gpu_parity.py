@@ -399,3 +399,19 @@ def check_tree_outputs(T, acc, inter, theta):
     assert np.array_equal(g.view(np.uint32), r_acc.view(np.uint32))
     gi = u32(inter)[T.perm]
     assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)
+
+
+def test_allocation_failure_is_reported_and_recovered(tt, monkeypatch):
+    # the workspace must grow for this call; the hook makes that allocation fail
+    pos, mass = plummer(3_000_000, 3)
+    p, m = dev(pos), dev(mass)
+    monkeypatch.setenv("ORRERY_FAIL_ALLOC", "1")
+    with pytest.raises(tt.OrreryError) as e:
+        tt.bh_forces(p, m)
+    assert e.value.status == -6
+    monkeypatch.delenv("ORRERY_FAIL_ALLOC")
+    # nothing was left half-built: a small call and then the large one succeed
+    small = case("plummer_4096")
+    check_forces(tt, small[0], small[1], small[2], small[3], 0.5, "coherent")
+    acc, inter, vis = tt.bh_forces(p, m, counters=False)
+    assert bool(torch.isfinite(acc).all())

@@ -202,7 +202,9 @@ int get_workspace(int64_t n, int64_t nodes, Workspace **out)
         w->cap_n = w->cap_nodes = -1;
         Buffers probe{};
         size_t bytes = carve(probe, nullptr, cn, cm);
-        if (cudaMalloc(&w->base, bytes) != cudaSuccess) {
+        // ORRERY_FAIL_ALLOC=1 makes this allocation fail (failure-path tests)
+        const char *fail = getenv("ORRERY_FAIL_ALLOC");
+        if ((fail && fail[0] == '1') || cudaMalloc(&w->base, bytes) != cudaSuccess) {
             cudaGetLastError();
             w->base = nullptr;
             return ORRERY_ENOMEM;
