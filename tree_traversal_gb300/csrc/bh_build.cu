@@ -228,9 +228,8 @@ void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &
     g_launches += 1;
 }
 
-void launch_moments(int32_t leaf_cap, const Buffers &b, cudaStream_t st)
+void launch_moments(const Buffers &b, cudaStream_t st)
 {
-    (void)leaf_cap;
     cudaMemsetAsync(b.arrive, 0, sizeof(int32_t) * (size_t)b.max_nodes, st);
     k_moments<<<ceil_div(b.n, kThreads), kThreads, 0, st>>>(b.ps, b.n, b.ncount, b.node_start,
                                                            b.meta, b.parent, b.nchild, b.arrive,

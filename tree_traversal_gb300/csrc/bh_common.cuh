@@ -10,7 +10,6 @@
 namespace obh {
 
 constexpr int kLevels = 21;          // bits per axis; deepest octree level
-constexpr int kWarp = 32;
 
 // Bits of the device status word.
 constexpr int kStatusNonFinite = 1;  // a position or mass is not finite
@@ -75,14 +74,12 @@ void launch_gather(const float *pos, const float *mass, const uint32_t *perm, co
                    cudaStream_t st);
 void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b,
                   cudaStream_t st);
-void launch_moments(int32_t leaf_cap, const Buffers &b, cudaStream_t st);
+void launch_moments(const Buffers &b, cudaStream_t st);
 // a7 with the a8 scatter fused: results land in the caller's order
 void launch_walk(int traversal, float theta, float eps, const uint32_t *perm, const Buffers &b,
                  float *acc, uint32_t *inter, uint32_t *visits, cudaStream_t st);
 void launch_direct(const float *pos, const float *mass, int64_t n, float eps, float *acc,
                    int *status, cudaStream_t st);
-void launch_scan_u32(const uint32_t *in, uint32_t *out, int64_t count, uint32_t *partial,
-                     cudaStream_t st);
 void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *partial,
                     cudaStream_t st);
 int64_t scan_partial_count(int64_t count);
@@ -99,9 +96,6 @@ __device__ __forceinline__ int common_levels(uint64_t a, uint64_t b)
     int msb = 63 - __clzll((long long)x);
     return (kLevels - 1) - msb / 3;
 }
-
-__device__ __forceinline__ float4 ldg_f4(const float4 *p) { return __ldg(p); }
-__device__ __forceinline__ int4 ldg_i4(const int4 *p) { return __ldg(p); }
 
 inline unsigned ceil_div(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b); }
 

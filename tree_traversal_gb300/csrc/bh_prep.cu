@@ -188,7 +188,7 @@ k_gather(const float *__restrict__ pos, const float *__restrict__ mass,
                         __ldg(pos + 3 * (int64_t)i + 2), __ldg(mass + i));
 }
 
-// ---- exclusive scan of uint32 (three launches, no inter-block waiting) ----
+// ---- exclusive scan into uint32 (three launches, no inter-block waiting) ----
 constexpr int kScanThreads = 256;
 constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;
@@ -285,12 +285,6 @@ static void scan_exclusive(const T *in, uint32_t *out, int64_t count, uint32_t *
     k_scan_partials<<<1, kScanThreads, 0, st>>>(partial, parts);
     k_scan_down<T><<<(unsigned)parts, kScanThreads, 0, st>>>(in, out, count, partial);
     g_launches += 3;
-}
-
-void launch_scan_u32(const uint32_t *in, uint32_t *out, int64_t count, uint32_t *partial,
-                     cudaStream_t st)
-{
-    scan_exclusive<uint32_t>(in, out, count, partial, st);
 }
 
 void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *partial,
