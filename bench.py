@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=8.0,
                    help="target wall time of the CPU-oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--scaling", action="store_true",
+                   help="instead of the benchmark line, the pages' scaling study: one JSON "
+                        "line per N from 1024 to 16M particles")
     p.add_argument("--crossover", action="store_true",
                    help="instead of the benchmark line, time the tree against direct "
                         "summation over a range of N (one JSON line per N)")
@@ -72,6 +75,57 @@ def replica_throughput(local_ms: float, local_units: float, steps: int, dist=Non
         total_ms, units = float(mx[0].item()), float(t[1].item())
     ms_per_step = total_ms / steps
     return ms_per_step, units / (ms_per_step / 1000.0)
+
+
+def run_scaling(args) -> None:
+    """The pages' "Scaling, and where it stops" table on this GPU: whole
+    evaluation and walk per N, ms / (N log2 N), the local exponent, and the
+    interaction and visit counts per particle (median of --steps calls)."""
+    import math
+
+    import torch
+
+    import tree_traversal_gb300 as tt
+    from inputs import plummer
+    from tree_traversal_gb300.build import build
+
+    build()
+    tt.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    prev = None
+    sizes = [1024 << k for k in range(12)] + [4194304, 8388608, 16777216]
+    for n in sizes:
+        pos_np, mass_np = plummer(n)
+        pos = torch.from_numpy(pos_np).to(dev)
+        mass = torch.from_numpy(mass_np).to(dev)
+        acc = torch.empty((n, 3), device=dev)
+        inter = torch.empty((n, 2), dtype=torch.int32, device=dev)
+        vis = torch.empty(n, dtype=torch.int32, device=dev)
+        total, walk = [], []
+        for it in range(args.warmup + args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            tt.bh_forces(pos, mass, 0.5, 0.05, 32, args.traversal, out=(acc, inter, vis))
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            if it >= args.warmup:
+                total.append(a.elapsed_time(b))
+                walk.append(tt.last_timings()["walk_ms"])
+        t = statistics.median(total)
+        tm = tt.last_timings()
+        row = {"n": n, "total_ms": t, "walk_ms": statistics.median(walk),
+               "spread": (max(total) - min(total)) / t,
+               "ms_per_nlogn": t / (n * math.log2(n)),
+               "exponent": (math.log(t / prev[1]) / math.log(n / prev[0])) if prev else None,
+               "cells_per_particle": float(inter[:, 0].double().mean()),
+               "interactions_per_particle": float(inter.double().sum(1).mean()),
+               "visits_per_particle": float(vis.double().mean()),
+               "nodes": tm["num_nodes"], "depth": tm["depth"], "traversal": args.traversal}
+        prev = (n, t)
+        print(json.dumps(row), flush=True)
+        del pos, mass, acc, inter, vis
+        torch.cuda.empty_cache()
 
 
 def run_crossover(args) -> None:
@@ -264,6 +318,9 @@ def main():
         return
     if args.crossover:
         run_crossover(args)
+        return
+    if args.scaling:
+        run_scaling(args)
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

@@ -319,6 +319,13 @@ def test_full_size_plummer_1m(tt):
     check_full_size(tt, pos, mass, [0.5])
 
 
+def test_beyond_the_configs_8m_plummer(tt):
+    # eight times the largest single sphere of the configurations: the whole
+    # tree bit-exact, sampled warps of targets bit-exact
+    pos, mass = plummer(8 * 1048576, PAGES_SEED + 8)
+    check_full_size(tt, pos, mass, [0.5])
+
+
 def test_full_size_two_spheres_theta_sweep(tt):
     pos, mass = two_spheres(1048576)
     check_full_size(tt, pos, mass, [0.3, 0.5, 0.7])
