@@ -409,9 +409,10 @@ def check_tree_outputs(T, acc, inter, theta):
 
 
 def test_allocation_failure_is_reported_and_recovered(tt, monkeypatch):
-    # the workspace must grow for this call; the hook makes that allocation fail
+    # after a release the next call must allocate; the hook makes that fail
     pos, mass = plummer(3_000_000, 3)
     p, m = dev(pos), dev(mass)
+    tt.release()
     monkeypatch.setenv("ORRERY_FAIL_ALLOC", "1")
     with pytest.raises(tt.OrreryError) as e:
         tt.bh_forces(p, m)
