@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=8.0,
                    help="target wall time of the CPU-oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--fast-term", action="store_true",
+                   help="time the approximate inverse square root (ORRERY_FAST_TERM) instead of "
+                        "the bit-reproducible term")
     p.add_argument("--scaling", action="store_true",
                    help="instead of the benchmark line, the pages' scaling study: one JSON "
                         "line per N from 1024 to 16M particles")
@@ -354,7 +357,7 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     call = lambda trav: tt.bh_forces(pos, mass, params["theta"], params["eps"], params["leaf_cap"],
-                                     trav, out=(acc, inter, visits))
+                                     trav, out=(acc, inter, visits), fast_term=args.fast_term)
 
     # untimed: the comparison traversal (its visits give the redundancy ratio)
     other = "independent" if args.traversal != "independent" else "coherent"
@@ -441,6 +444,8 @@ def main():
         "config": {"workload": args.workload, "n": n, "theta": params["theta"],
                    "eps": params["eps"], "leaf_cap": params["leaf_cap"],
                    "traversal": args.traversal, "parallelism": "replicas" if world > 1 else "1gpu",
+                   "term": "fast (approximate inverse root)" if args.fast_term
+                   else "bit-reproducible (Newton inverse root)",
                    "l2": "flushed between steps (256 MiB write outside the step events)"},
         "gpu_launches": int(launches),
         "clocks": {"sm_mhz": csum["sm_mhz"], "sm_max_mhz": csum["sm_max_mhz"],

@@ -76,6 +76,8 @@ def test_argument_checks_answer_on_the_host(lib):
     assert f(dummy, dummy, 10, 0.5, 0.05, 0, 1, dummy, P, P, P) == L.EINVAL
     assert f(dummy, dummy, 10, 0.5, 0.05, 32, 7, dummy, P, P, P) == L.EINVAL
     assert f(dummy, dummy, 10, 0.5, 0.05, 32, 6, dummy, P, P, P) == L.EINVAL
+    assert f(dummy, dummy, 10, 0.5, 0.05, 32, 0x201, dummy, P, P, P) == L.EINVAL
+    assert f(dummy, dummy, 10, 0.5, 0.05, 32, 0x106, dummy, P, P, P) == L.EINVAL
     assert f(dummy, dummy, 10, 0.5, 0.05, 32, -1, dummy, P, P, P) == L.EINVAL
     assert f(P, dummy, 10, 0.5, 0.05, 32, 1, dummy, P, P, P) == L.EINVAL
     assert f(dummy, dummy, 10, 0.5, 0.05, 32, 1, P, P, P, P) == L.EINVAL

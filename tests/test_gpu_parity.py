@@ -423,3 +423,32 @@ def test_allocation_failure_is_reported_and_recovered(tt, monkeypatch):
     check_forces(tt, small[0], small[1], small[2], small[3], 0.5, "coherent")
     acc, inter, vis = tt.bh_forces(p, m, counters=False)
     assert bool(torch.isfinite(acc).all())
+
+
+# ---------------------------------------------------------------------------
+# the opt-in fast term: same decisions and counts, accelerations within 1e-5
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("traversal", ["coherent", "independent", "coherent64"])
+@pytest.mark.parametrize("name", ["plummer_4096", "plummer_131072", "duplicates_65",
+                                  "unequal_masses_cap16", "two_spheres_2x8192"])
+def test_fast_term_within_tolerance(tt, name, traversal):
+    pos, mass, cap, T = case(name)
+    acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), 0.5, EPS, cap, traversal, fast_term=True)
+    r_acc, r_pc, r_pp, r_vis = T.walk(0.5, EPS, threads=oracle.default_threads())
+    g = acc.cpu().numpy()[T.perm]
+    ok = np.linalg.norm(r_acc.astype(np.float64), axis=1) > 0
+    assert oracle.relative_error(g[ok], r_acc[ok]).max() <= REL_TOL
+    assert np.array_equal(g[~ok], r_acc[~ok])
+    gi = u32(inter)[T.perm]
+    assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)
+
+
+def test_fast_term_full_size_all_targets(tt):
+    pos, mass = plummer(1048576, PAGES_SEED)
+    T = oracle.Tree(pos, mass, 32)
+    acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), 0.5, EPS, 32, "coherent", fast_term=True)
+    r_acc, r_pc, r_pp, _ = T.walk(0.5, EPS, threads=oracle.default_threads())
+    g = acc.cpu().numpy()[T.perm]
+    assert oracle.relative_error(g, r_acc).max() <= REL_TOL
+    gi = u32(inter)[T.perm]
+    assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)

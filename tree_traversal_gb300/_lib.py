@@ -30,6 +30,7 @@ COHERENT_16 = 2
 COHERENT_64 = 3
 DESCEND_TOGETHER = 4
 COHERENT_BALLOT = 5
+FAST_TERM = 0x100
 # coherence width of each traversal (targets sharing one node index)
 WIDTH = {INDEPENDENT: 1, COHERENT: 32, COHERENT_16: 16, COHERENT_64: 64, DESCEND_TOGETHER: 32,
          COHERENT_BALLOT: 32}

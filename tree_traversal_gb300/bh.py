@@ -43,14 +43,17 @@ def _ptr(t):
 
 
 def bh_forces(pos: torch.Tensor, mass: torch.Tensor, theta: float = 0.5, eps: float = 0.05,
-              leaf_cap: int = 32, traversal="coherent", counters: bool = True, out=None):
+              leaf_cap: int = 32, traversal="coherent", counters: bool = True, out=None,
+              fast_term: bool = False):
     """Accelerations of n particles (caller order) on the current CUDA stream.
 
     pos [n, 3] float32, mass [n] float32, both CUDA and contiguous.
     Returns (acc [n, 3] float32, interactions [n, 2] int32 {particle-cell,
     particle-particle} or None, visits [n] int32 or None); the counters are
     uint32 values stored in int32 tensors (they never exceed 2^31).
-    ``out`` may pass preallocated (acc, interactions, visits) tensors."""
+    ``out`` may pass preallocated (acc, interactions, visits) tensors.
+    ``fast_term`` selects the approximate inverse square root (ORRERY_FAST_TERM):
+    faster, equal to the exact path to rounding rather than bit for bit."""
     n = int(pos.shape[0]) if pos.dim() == 2 else -1
     _check_device(pos, "pos", (n, 3))
     _check_device(mass, "mass", (n,))
@@ -71,7 +74,8 @@ def bh_forces(pos: torch.Tensor, mass: torch.Tensor, theta: float = 0.5, eps: fl
     with torch.cuda.device(dev):
         rc = _lib.load().orrery_bh_forces(
             _ptr(pos), _ptr(mass), n, float(theta), float(eps), int(leaf_cap),
-            _traversal(traversal), _ptr(acc), _ptr(inter), _ptr(visits), _stream_handle(dev))
+            _traversal(traversal) | (_lib.FAST_TERM if fast_term else 0), _ptr(acc), _ptr(inter),
+            _ptr(visits), _stream_handle(dev))
     if rc != _lib.OK:
         raise _lib.OrreryError(rc, "orrery_bh_forces")
     return acc, inter, visits

@@ -223,7 +223,9 @@ int check_args(int64_t n, float theta, float eps, int32_t leaf_cap, int32_t trav
     if (n < 0 || n > kMaxN) return ORRERY_EINVAL;
     if (!(theta >= 0.0f) || !(eps >= 0.0f)) return ORRERY_EINVAL;  // also rejects NaN
     if (leaf_cap < 1) return ORRERY_EINVAL;
-    if (traversal < ORRERY_INDEPENDENT || traversal > ORRERY_COHERENT_BALLOT) return ORRERY_EINVAL;
+    const int walk = traversal & kTraversalMask;
+    if ((traversal & ~(kTraversalMask | kFastTermFlag)) != 0) return ORRERY_EINVAL;
+    if (walk < ORRERY_INDEPENDENT || walk > ORRERY_COHERENT_BALLOT) return ORRERY_EINVAL;
     if (node_bound(n, leaf_cap) > (int64_t)INT32_MAX) return ORRERY_ERANGE;
     return ORRERY_OK;
 }

@@ -11,6 +11,11 @@ namespace obh {
 
 constexpr int kLevels = 21;          // bits per axis; deepest octree level
 
+// The traversal argument: the low byte selects the walk, a flag bit the fast
+// force term (see include/orrery_bh.h).
+constexpr int kTraversalMask = 0xff;
+constexpr int kFastTermFlag = 0x100;
+
 // Bits of the device status word.
 constexpr int kStatusNonFinite = 1;  // a position or mass is not finite
 constexpr int kStatusWalkBound = 2;  // a walk hit its iteration bound

@@ -117,7 +117,8 @@ extern "C" int orrery_bh_forces_noalloc(const float *pos_d, const float *mass_d,
                                         uint32_t *visits_d, void *stream)
 {
     if (n < 0 || n > kMaxN || !(theta >= 0.0f) || !(eps >= 0.0f) || leaf_cap < 1 ||
-        traversal < ORRERY_INDEPENDENT || traversal > ORRERY_COHERENT_BALLOT)
+        (traversal & ~(kTraversalMask | kFastTermFlag)) != 0 ||
+        (traversal & kTraversalMask) > ORRERY_COHERENT_BALLOT)
         return ORRERY_EINVAL;
     if (n == 0) return ORRERY_OK;
     if (!pos_d || !mass_d || !acc_d) return ORRERY_EINVAL;

@@ -99,11 +99,21 @@ __device__ __forceinline__ float rsqrt_newton(float x)
     return y;
 }
 
+// kFast selects the hardware approximate inverse square root (rsqrtf, a few
+// ulp) in place of the Newton sequence: faster, no longer reproducible bit for
+// bit on a CPU (the caller opts in with ORRERY_FAST_TERM).
+template <bool kFast>
+__device__ __forceinline__ float inv_sqrt(float x)
+{
+    return kFast ? rsqrtf(x) : rsqrt_newton(x);
+}
+
+template <bool kFast>
 __device__ __forceinline__ void add_term(float dx, float dy, float dz, float d2, float m,
                                          float eps2, float &ax, float &ay, float &az)
 {
     const float r2 = __fadd_rn(d2, eps2);
-    const float y = rsqrt_newton(r2);
+    const float y = inv_sqrt<kFast>(r2);
     const float f = __fmul_rn(__fmul_rn(m, y), __fmul_rn(y, y));
     ax = __fmaf_rn(f, dx, ax);
     ay = __fmaf_rn(f, dy, ay);
@@ -115,17 +125,19 @@ __device__ __forceinline__ float dist2(float dx, float dy, float dz)
     return __fmaf_rn(dz, dz, __fmaf_rn(dy, dy, __fmul_rn(dx, dx)));
 }
 
+template <bool kFast>
 __device__ __forceinline__ void particle_term(const float4 &p, const float4 &xi, float eps2,
                                               float &ax, float &ay, float &az)
 {
     const float dx = __fsub_rn(p.x, xi.x);
     const float dy = __fsub_rn(p.y, xi.y);
     const float dz = __fsub_rn(p.z, xi.z);
-    add_term(dx, dy, dz, dist2(dx, dy, dz), p.w, eps2, ax, ay, az);
+    add_term<kFast>(dx, dy, dz, dist2(dx, dy, dz), p.w, eps2, ax, ay, az);
 }
 
 // Block prologue shared by both kernels: status, node count and whether the
 // self term may be summed (see the file comment). Returns false to skip.
+template <bool kFast>
 __device__ __forceinline__ bool prologue(const WalkArgs &a, int &num_nodes, bool &self_free)
 {
     __shared__ int s_state[3];
@@ -135,7 +147,7 @@ __device__ __forceinline__ bool prologue(const WalkArgs &a, int &num_nodes, bool
         s_state[1] = P->num_nodes;
         bool ok = a.eps2 > 0.0f;
         if (ok) {
-            const float y = rsqrt_newton(a.eps2);
+            const float y = inv_sqrt<kFast>(a.eps2);
             const float f = __fmul_rn(__fmul_rn(P->mmax, y), __fmul_rn(y, y));
             ok = isfinite(f);
         }
@@ -168,7 +180,7 @@ struct Group {
 // of an accepted ancestor of k, which is never below escape(k) -- so the
 // ballot form visits exactly the same union; it is kept to measure the cost
 // of the two instructions against each other.
-template <int W, bool kCount, bool kSelfFree, bool kBallot = false>
+template <int W, bool kCount, bool kSelfFree, bool kBallot, bool kFast>
 __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, float4 *stage)
 {
     constexpr int G = Group<W>::G;
@@ -219,7 +231,7 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
                 const float dz = __fsub_rn(c.z, xi[i].z);
                 const float d2 = dist2(dx, dy, dz);
                 if (__int_as_float(w.w) < __fmul_rn(a.theta2, d2)) {
-                    add_term(dx, dy, dz, d2, c.w, a.eps2, ax[i], ay[i], az[i]);
+                    add_term<kFast>(dx, dy, dz, d2, c.w, a.eps2, ax[i], ay[i], az[i]);
                     if (kCount) ++pc[i];
                     next[i] = w.x;
                 } else {
@@ -251,11 +263,11 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
                     if (kSelfFree) {
 #pragma unroll 4
                         for (int j = 0; j < chunk; ++j)
-                            particle_term(stage[j], xi[i], a.eps2, ax[i], ay[i], az[i]);
+                            particle_term<kFast>(stage[j], xi[i], a.eps2, ax[i], ay[i], az[i]);
                     } else {
                         const int self = tgt[i] - (first + b);
                         for (int j = 0; j < chunk; ++j)
-                            if (j != self) particle_term(stage[j], xi[i], a.eps2, ax[i], ay[i], az[i]);
+                            if (j != self) particle_term<kFast>(stage[j], xi[i], a.eps2, ax[i], ay[i], az[i]);
                     }
                 }
                 __syncwarp(gmask);
@@ -268,19 +280,19 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
         if (valid[i]) store_target<kCount>(a, tgt[i], ax[i], ay[i], az[i], pc[i], pp[i], steps);
 }
 
-template <int W, bool kCount, bool kBallot = false>
+template <int W, bool kCount, bool kBallot, bool kFast>
 __global__ void __launch_bounds__(kThreads) k_walk_coherent(WalkArgs a)
 {
     __shared__ float4 s_leaf[kWarpsPerBlock][32];
     int num_nodes;
     bool self_free;
-    if (!prologue(a, num_nodes, self_free)) return;  // block-uniform
+    if (!prologue<kFast>(a, num_nodes, self_free)) return;  // block-uniform
     constexpr int G = Group<W>::G;
     float4 *stage = &s_leaf[threadIdx.x >> 5][(threadIdx.x & 31) & ~(G - 1)];
     if (self_free)
-        coherent_walk<W, kCount, true, kBallot>(a, num_nodes, stage);
+        coherent_walk<W, kCount, true, kBallot, kFast>(a, num_nodes, stage);
     else
-        coherent_walk<W, kCount, false, kBallot>(a, num_nodes, stage);
+        coherent_walk<W, kCount, false, kBallot, kFast>(a, num_nodes, stage);
 }
 
 // The scheme the pages reject, kept as a measured contrast (ADR-0029,
@@ -290,7 +302,7 @@ __global__ void __launch_bounds__(kThreads) k_walk_coherent(WalkArgs a)
 // otherwise a leaf is opened for every target and an internal node is
 // entered by all. Each target's sum depends on which targets share its warp,
 // so this is a different function of the input from the walks above.
-template <bool kCount, bool kSelfFree>
+template <bool kCount, bool kSelfFree, bool kFast>
 __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, float4 *stage)
 {
     const int lane = threadIdx.x & 31;
@@ -310,7 +322,7 @@ __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, 
         const bool accept = __int_as_float(w.w) < __fmul_rn(a.theta2, d2);
         if (__all_sync(0xffffffffu, accept || !valid)) {
             if (valid) {
-                add_term(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
+                add_term<kFast>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
                 if (kCount) ++pc;
             }
             k = w.x;
@@ -330,11 +342,11 @@ __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, 
                     if (kSelfFree) {
 #pragma unroll 4
                         for (int j = 0; j < chunk; ++j)
-                            particle_term(stage[j], xi, a.eps2, ax, ay, az);
+                            particle_term<kFast>(stage[j], xi, a.eps2, ax, ay, az);
                     } else {
                         const int self = t - (first + b);
                         for (int j = 0; j < chunk; ++j)
-                            if (j != self) particle_term(stage[j], xi, a.eps2, ax, ay, az);
+                            if (j != self) particle_term<kFast>(stage[j], xi, a.eps2, ax, ay, az);
                     }
                 }
                 __syncwarp();
@@ -348,21 +360,21 @@ __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, 
     if (valid) store_target<kCount>(a, t, ax, ay, az, pc, pp, steps);
 }
 
-template <bool kCount>
+template <bool kCount, bool kFast>
 __global__ void __launch_bounds__(kThreads) k_walk_together(WalkArgs a)
 {
     __shared__ float4 s_leaf[kWarpsPerBlock][32];
     int num_nodes;
     bool self_free;
-    if (!prologue(a, num_nodes, self_free)) return;  // block-uniform
+    if (!prologue<kFast>(a, num_nodes, self_free)) return;  // block-uniform
     float4 *stage = s_leaf[threadIdx.x >> 5];
     if (self_free)
-        together_walk<kCount, true>(a, num_nodes, stage);
+        together_walk<kCount, true, kFast>(a, num_nodes, stage);
     else
-        together_walk<kCount, false>(a, num_nodes, stage);
+        together_walk<kCount, false, kFast>(a, num_nodes, stage);
 }
 
-template <bool kCount, bool kSelfFree>
+template <bool kCount, bool kSelfFree, bool kFast>
 __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_nodes)
 {
     const int t = blockIdx.x * kThreads + threadIdx.x;
@@ -379,7 +391,7 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
         const float dz = __fsub_rn(c.z, xi.z);
         const float d2 = dist2(dx, dy, dz);
         if (__int_as_float(w.w) < __fmul_rn(a.theta2, d2)) {
-            add_term(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
+            add_term<kFast>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
             if (kCount) ++pc;
             k = w.x;
         } else if (w.z != 0) {
@@ -390,7 +402,7 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
             }
             if (kCount) pp += count - ((unsigned)(t - first) < (unsigned)count ? 1u : 0u);
             for (int j = first; j < first + count; ++j)
-                if (kSelfFree || j != t) particle_term(__ldg(a.ps + j), xi, a.eps2, ax, ay, az);
+                if (kSelfFree || j != t) particle_term<kFast>(__ldg(a.ps + j), xi, a.eps2, ax, ay, az);
             k = w.x;
         } else {
             k = k + 1;
@@ -400,23 +412,61 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
     store_target<kCount>(a, t, ax, ay, az, pc, pp, steps);
 }
 
-template <bool kCount>
+template <bool kCount, bool kFast>
 __global__ void __launch_bounds__(kThreads) k_walk_independent(WalkArgs a)
 {
     int num_nodes;
     bool self_free;
-    if (!prologue(a, num_nodes, self_free)) return;
+    if (!prologue<kFast>(a, num_nodes, self_free)) return;
     if (self_free)
-        independent_walk<kCount, true>(a, num_nodes);
+        independent_walk<kCount, true, kFast>(a, num_nodes);
     else
-        independent_walk<kCount, false>(a, num_nodes);
+        independent_walk<kCount, false, kFast>(a, num_nodes);
+}
+
+template <bool kFast>
+void launch_kernels(int traversal, bool count, unsigned grid, const WalkArgs &a, cudaStream_t st)
+{
+    // coherent groups of W targets: kThreads lanes cover kThreads * T targets
+    auto coherent = [&](auto wtag) {
+        constexpr int W = decltype(wtag)::value;
+        const unsigned g = ceil_div(a.n, (int64_t)kThreads * Group<W>::T);
+        if (count)
+            k_walk_coherent<W, true, false, kFast><<<g, kThreads, 0, st>>>(a);
+        else
+            k_walk_coherent<W, false, false, kFast><<<g, kThreads, 0, st>>>(a);
+    };
+    switch (traversal) {
+    case 1: coherent(std::integral_constant<int, 32>{}); break;
+    case 2: coherent(std::integral_constant<int, 16>{}); break;
+    case 3: coherent(std::integral_constant<int, 64>{}); break;
+    case 4:
+        if (count)
+            k_walk_together<true, kFast><<<grid, kThreads, 0, st>>>(a);
+        else
+            k_walk_together<false, kFast><<<grid, kThreads, 0, st>>>(a);
+        break;
+    case 5:
+        if (count)
+            k_walk_coherent<32, true, true, kFast><<<grid, kThreads, 0, st>>>(a);
+        else
+            k_walk_coherent<32, false, true, kFast><<<grid, kThreads, 0, st>>>(a);
+        break;
+    default:
+        if (count)
+            k_walk_independent<true, kFast><<<grid, kThreads, 0, st>>>(a);
+        else
+            k_walk_independent<false, kFast><<<grid, kThreads, 0, st>>>(a);
+    }
 }
 
 }  // namespace
 
-void launch_walk(int traversal, float theta, float eps, const uint32_t *perm, const Buffers &b,
-                 float *acc, uint32_t *inter, uint32_t *visits, cudaStream_t st)
+void launch_walk(int traversal_flags, float theta, float eps, const uint32_t *perm,
+                 const Buffers &b, float *acc, uint32_t *inter, uint32_t *visits, cudaStream_t st)
 {
+    const int traversal = traversal_flags & kTraversalMask;
+    const bool fast = (traversal_flags & kFastTermFlag) != 0;
     const bool count = inter != nullptr || visits != nullptr;
     WalkArgs a;
     a.ps = b.ps;
@@ -431,37 +481,10 @@ void launch_walk(int traversal, float theta, float eps, const uint32_t *perm, co
     a.inter = inter;
     a.visits = visits;
     const unsigned grid = ceil_div(b.n, kThreads);
-    // coherent groups of W targets: kThreads lanes cover kThreads * T targets
-    auto coherent = [&](auto wtag) {
-        constexpr int W = decltype(wtag)::value;
-        const unsigned g = ceil_div(b.n, (int64_t)kThreads * Group<W>::T);
-        if (count)
-            k_walk_coherent<W, true><<<g, kThreads, 0, st>>>(a);
-        else
-            k_walk_coherent<W, false><<<g, kThreads, 0, st>>>(a);
-    };
-    switch (traversal) {
-    case 1: coherent(std::integral_constant<int, 32>{}); break;
-    case 2: coherent(std::integral_constant<int, 16>{}); break;
-    case 3: coherent(std::integral_constant<int, 64>{}); break;
-    case 4:
-        if (count)
-            k_walk_together<true><<<grid, kThreads, 0, st>>>(a);
-        else
-            k_walk_together<false><<<grid, kThreads, 0, st>>>(a);
-        break;
-    case 5:
-        if (count)
-            k_walk_coherent<32, true, true><<<grid, kThreads, 0, st>>>(a);
-        else
-            k_walk_coherent<32, false, true><<<grid, kThreads, 0, st>>>(a);
-        break;
-    default:
-        if (count)
-            k_walk_independent<true><<<grid, kThreads, 0, st>>>(a);
-        else
-            k_walk_independent<false><<<grid, kThreads, 0, st>>>(a);
-    }
+    if (fast)
+        launch_kernels<true>(traversal, count, grid, a, st);
+    else
+        launch_kernels<false>(traversal, count, grid, a, st);
     g_launches += 1;
 }
 
