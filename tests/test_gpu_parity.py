@@ -9,7 +9,7 @@ binary32 operations, in the same order):
   * accelerations: bit-exact, and in any case within 1e-5 max relative error
     (the stated tolerance);
   * the coherent and the independent walk: bit-identical to each other.
-Sizes span several radix tiles (4096 keys) and scan tiles (2048 entries) with
+Sizes span several radix tiles and scan tiles (2048 entries each) with
 ragged tails; the full-size workloads (1M Plummer, two 1M spheres swept over
 theta) are compared over the whole tree and on sampled warps of targets.
 """
@@ -90,7 +90,7 @@ CASES = {
     "unequal_masses_cap16": lambda: _masses(9000, 12),
     "uniform_20000_cap200": lambda: (*uniform_cube(20000, 6), 200),
     "two_spheres_2x8192": lambda: (*two_spheres(8192), 32),
-    # sizes on the radix tile (4096 keys) and scan tile (2048 entries) edges
+    # sizes on the radix tile and scan tile (2048 entries each) edges
     "edge_2047": lambda: (*plummer(2047, 91), 32),
     "edge_4095": lambda: (*plummer(4095, 92), 32),
     "edge_8193_cap3": lambda: (*plummer(8193, 93), 3),

@@ -6,7 +6,7 @@
 // first thing to do about it. Seven passes of 9 bits cover the 63-bit keys.
 // Each pass is three launches with no inter-block waiting: per-tile digit
 // counts, a per-digit scan over tiles, and a stable scatter. The scatter
-// ranks every key of its 4096-key tile (each warp walks a contiguous 512-key
+// ranks every key of its 2048-key tile (each warp walks a contiguous 256-key
 // span 32 keys at a time, ranking equal digits with a match-any vote), puts
 // the tile in digit order in shared memory, and then writes each digit's run
 // to its global slot with consecutive threads on consecutive addresses.
@@ -17,9 +17,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 16;                      // per lane
-constexpr int kTile = kThreads * kItems;        // 4096 keys per block
-constexpr int kWarpSpan = 32 * kItems;          // 512 consecutive keys per warp
+constexpr int kItems = 8;                       // per lane
+constexpr int kTile = kThreads * kItems;        // 2048 keys per block
+constexpr int kWarpSpan = 32 * kItems;          // 256 consecutive keys per warp
 constexpr int kBits = 9;
 constexpr int kBins = 1 << kBits;               // 512 digits
 constexpr int kPasses = 7;                      // 7 x 9 = 63 key bits
