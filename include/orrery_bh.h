@@ -51,7 +51,10 @@ extern "C" {
 
 #define ORRERY_OK 0
 #define ORRERY_EINVAL (-1)     /* bad argument; nothing was launched */
-#define ORRERY_ENONFINITE (-2) /* a position or mass is NaN or infinite */
+#define ORRERY_ENONFINITE (-2) /* a position or mass is NaN or infinite, a coordinate
+                                  has magnitude 2^125 or more, or a cell's mass moments
+                                  overflow binary32 (the supported range keeps every
+                                  separation the walk forms finite) */
 #define ORRERY_ERANGE (-3)     /* node count or size beyond the int32 range */
 #define ORRERY_ECUDA (-4)      /* a CUDA runtime call failed */
 #define ORRERY_EWALK (-5)      /* a walk exceeded its iteration bound */
@@ -198,7 +201,9 @@ int orrery_bh_tree(const float *pos_d, const float *mass_d, int64_t n, int32_t l
  * beat"): acc_i = sum over j != i, j ascending in caller order, of the tree's
  * particle term (same softening and arithmetic, no approximation). O(n^2).
  *   pos_d [n][3], mass_d [n], acc_d [n][3]: device float32, caller order.
- * Returns ORRERY_OK, ORRERY_EINVAL, ORRERY_ENONFINITE or ORRERY_ECUDA.
+ * Returns ORRERY_OK, ORRERY_EINVAL, ORRERY_ENONFINITE (here only for a NaN or
+ * infinite position or mass: the range limit of the tree does not apply) or
+ * ORRERY_ECUDA.
  */
 int orrery_direct_forces(const float *pos_d, const float *mass_d, int64_t n, float eps,
                          float *acc_d, void *stream);

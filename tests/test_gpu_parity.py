@@ -190,15 +190,25 @@ def test_empty_input(tt):
 
 def test_nonfinite_input_is_reported(tt):
     pos, mass = plummer(3000, 1)
-    for bad in ("pos", "mass"):
+    for bad in ("pos", "mass", "range", "moment"):
         p, m = pos.copy(), mass.copy()
         if bad == "pos":
             p[1234, 1] = np.nan
-        else:
+        elif bad == "mass":
             m[17] = np.inf
-        with pytest.raises(tt.OrreryError) as e:
-            tt.bh_forces(dev(p), dev(m))
-        assert e.value.status == -2
+        elif bad == "range":  # a coordinate of 2^125: outside the supported range
+            p[5, 2] = np.float32(2.0 ** 125)
+        else:  # finite inputs whose mass moment overflows binary32
+            p *= np.float32(1e20)
+            m[:] = np.float32(1e30)
+        for trav in ("coherent", "independent"):
+            with pytest.raises(tt.OrreryError) as e:
+                tt.bh_forces(dev(p), dev(m), traversal=trav)
+            assert e.value.status == -2, (bad, trav)
+    # just inside the range the call succeeds
+    p = pos.copy()
+    p[5, 2] = np.float32(np.nextafter(np.float32(2.0 ** 125), np.float32(0)))
+    tt.bh_forces(dev(p), dev(mass))
     # the library recovers: the next valid call is exact again
     pos, mass, cap, T = case("plummer_4096")
     check_forces(tt, pos, mass, cap, T, 0.5, "coherent")
@@ -452,3 +462,47 @@ def test_fast_term_full_size_all_targets(tt):
     assert oracle.relative_error(g, r_acc).max() <= REL_TOL
     gi = u32(inter)[T.perm]
     assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)
+
+
+# ---------------------------------------------------------------------------
+# a seeded sweep over sizes, leaf capacities, opening angles, softenings,
+# mass spreads and traversals: every output bit-exact against the oracle
+# ---------------------------------------------------------------------------
+def _random_config(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 30000))
+    cap = int(rng.choice([1, 2, 3, 8, 16, 32, 33, 64, 100]))
+    theta = float(rng.choice([0.0, 0.2, 0.5, 0.577, 0.8, 1.2]))
+    eps = float(rng.choice([0.0, 0.01, 0.05, 0.3]))
+    kind = int(rng.integers(0, 3))
+    if kind == 0:
+        pos, mass = plummer(n, 7000 + seed)
+    elif kind == 1:
+        pos, mass = uniform_cube(n, 7000 + seed, -float(rng.uniform(0.1, 100)), float(rng.uniform(0.1, 100)))
+    else:  # a few clustered blobs with repeated points
+        c = rng.normal(size=(5, 3)) * 10
+        pos = (c[rng.integers(0, 5, n)] + rng.normal(size=(n, 3)) * rng.choice([1e-3, 0.1, 1.0])).astype(np.float32)
+        pos[rng.random(n) < 0.05] = pos[0]
+        mass = np.full(n, np.float32(1.0 / n), np.float32)
+    if rng.random() < 0.5:
+        mass = (mass * rng.uniform(0.01, 10.0, n)).astype(np.float32)
+    trav = str(rng.choice(["coherent", "independent", "coherent16", "coherent64", "ballot"]))
+    return pos, mass, cap, theta, eps, trav
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_configurations_bit_exact(tt, seed):
+    pos, mass, cap, theta, eps, trav = _random_config(seed)
+    T = oracle.Tree(pos, mass, cap)
+    check_tree(tt, pos, mass, cap, T)
+    acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), theta, eps, cap, trav)
+    r_acc, r_pc, r_pp, r_vis = T.walk(theta, eps, threads=oracle.default_threads())
+    g = acc.cpu().numpy()[T.perm]
+    nan = np.isnan(r_acc)  # eps = 0 with coincident points: singular on both sides
+    assert np.array_equal(np.isnan(g), nan)
+    assert np.array_equal(g[~nan].view(np.uint32), r_acc[~nan].view(np.uint32))
+    gi = u32(inter)[T.perm]
+    assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)
+    width = {"independent": 1, "coherent": 32, "coherent16": 16, "coherent64": 64, "ballot": 32}[trav]
+    want = r_vis if width == 1 else np.repeat(T.group_visits(theta, eps, width), width)[: T.n]
+    assert np.array_equal(u32(vis)[T.perm], want)

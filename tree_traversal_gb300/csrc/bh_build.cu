@@ -20,6 +20,8 @@
 //    level-D cell around them is over capacity; the chain stops at the first
 //    level whose cell does not contain key[i + leaf_cap] (or at level 21).
 // escape(node) = scan value at the first position past the node's range.
+#include <cfloat>
+
 #include "bh_common.cuh"
 
 namespace obh {
@@ -127,8 +129,11 @@ k_build_emit(const uint64_t *__restrict__ K, int64_t n, const int8_t *__restrict
     atomicMax(&P->depth, first_level + cnt - 1);
 }
 
+// A node whose mass is not finite or whose CoM lies at 2^126 or beyond is
+// reported as non-finite: with every coordinate below 2^125 (checked with the
+// bounding box), every separation the walks form is then a finite number.
 __device__ __forceinline__ void store_moments(int64_t k, float sx, float sy, float sz, float M,
-                                              float4 *sums, float4 *com)
+                                              float4 *sums, float4 *com, DeviceParams *P)
 {
     __stcg(sums + k, make_float4(sx, sy, sz, M));
     float4 c = make_float4(0.0f, 0.0f, 0.0f, M);
@@ -137,6 +142,9 @@ __device__ __forceinline__ void store_moments(int64_t k, float sx, float sy, flo
         c.y = __fdiv_rn(sy, M);
         c.z = __fdiv_rn(sz, M);
     }
+    const float lim = 0x1p126f;
+    if (!(fabsf(M) <= FLT_MAX && fabsf(c.x) < lim && fabsf(c.y) < lim && fabsf(c.z) < lim))
+        atomicOr((int *)&P->status, kStatusNonFinite);
     __stcg(com + k, c);
 }
 
@@ -144,10 +152,10 @@ __device__ __forceinline__ void store_moments(int64_t k, float sx, float sy, flo
 // (0 for an internal node), bits of (side 2^-level)^2}.
 __device__ __forceinline__ void store_node(int64_t k, const int4 &m, bool leaf, float sx, float sy,
                                            float sz, float M, float4 *sums, float4 *com,
-                                           int4 *wnode, const DeviceParams *P)
+                                           int4 *wnode, DeviceParams *P)
 {
     wnode[k] = make_int4(m.x, m.y, leaf ? m.z : 0, __float_as_int(P->s2[m.w]));
-    store_moments(k, sx, sy, sz, M, sums, com);
+    store_moments(k, sx, sy, sz, M, sums, com, P);
 }
 
 // a6: one thread per leaf (the last node of each position's chain) sums its

@@ -84,7 +84,7 @@ k_bbox_partial(const float *__restrict__ pos, const float *__restrict__ mass, in
 #pragma unroll
         for (int a = 0; a < 3; ++a) {
             float x = __ldg(pos + 3 * i + a);
-            bad |= !isfinite(x);
+            bad |= !(fabsf(x) < 0x1p125f);  // non-finite, or beyond the supported range
             lo[a] = fminf(lo[a], x);
             hi[a] = fmaxf(hi[a], x);
         }

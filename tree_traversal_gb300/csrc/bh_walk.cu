@@ -159,18 +159,11 @@ __device__ __forceinline__ bool prologue(const WalkArgs &a, int &num_nodes, bool
     return s_state[0] == 0;
 }
 
-// One coherence group = W consecutive sorted targets sharing one node index.
-// W = 16: half a warp per group (two groups per warp, each advancing on its
-// own, like the pages' sub-group width of 16); W = 32: one warp; W = 64: one
-// warp with two targets per lane (the width the pages could not measure).
-// Lane l of a group holds targets base + i*G + l for i < T, with G lanes per
-// group and T targets per lane.
-template <int W>
-struct Group {
-    static constexpr int G = W < 32 ? W : 32;
-    static constexpr int T = W > 32 ? W / 32 : 1;
-};
-
+// One coherence group = W consecutive sorted targets sharing one node index,
+// one target per lane. W = 16: half a warp per group (two groups per warp,
+// each advancing on its own, like the pages' sub-group width of 16); W = 32:
+// one warp. (Width 64 -- two targets per lane -- is the packed walk below.)
+//
 // kBallot selects how the group finds its next node. The default takes the
 // minimum over the lanes' wanted indices (ADR-0029, Decision). The ballot form
 // (ADR-0029, Alternatives considered: "Vote on whether to descend, and
@@ -183,91 +176,61 @@ struct Group {
 template <int W, bool kCount, bool kSelfFree, bool kBallot, bool kFast>
 __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, float4 *stage)
 {
-    constexpr int G = Group<W>::G;
-    constexpr int T = Group<W>::T;
+    static_assert(W == 16 || W == 32, "one target per lane");
+    constexpr int G = W;
     const int lane = threadIdx.x & 31;
     const int glane = lane & (G - 1);
     const unsigned gmask = (G == 32) ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
-    const int base = ((blockIdx.x * kThreads + threadIdx.x) / G) * W;
-
-    int tgt[T], next[T];
-    bool valid[T];
-    float4 xi[T];
-    float ax[T], ay[T], az[T];
-    uint32_t pc[T], pp[T];
-#pragma unroll
-    for (int i = 0; i < T; ++i) {
-        tgt[i] = base + i * G + glane;
-        valid[i] = tgt[i] < a.n;
-        xi[i] = valid[i] ? __ldg(a.ps + tgt[i]) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        next[i] = valid[i] ? 0 : num_nodes;
-        ax[i] = ay[i] = az[i] = 0.0f;
-        pc[i] = pp[i] = 0;
-    }
+    const int tgt = blockIdx.x * kThreads + threadIdx.x;
+    const bool valid = tgt < a.n;
+    const float4 xi = valid ? __ldg(a.ps + tgt) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int next = valid ? 0 : num_nodes;
+    float ax = 0.0f, ay = 0.0f, az = 0.0f;
+    uint32_t pc = 0, pp = 0;
     int steps = 0;
-    int kb = __any_sync(gmask, valid[0]) ? 0 : num_nodes;  // the ballot form's node
+    int kb = __any_sync(gmask, valid) ? 0 : num_nodes;  // the ballot form's node
     for (; steps <= num_nodes; ++steps) {
-        int k;
-        if (kBallot) {
-            k = kb;
-        } else {
-            int v = next[0];
-#pragma unroll
-            for (int i = 1; i < T; ++i) v = min(v, next[i]);
-            k = __reduce_min_sync(gmask, v);
-        }
+        const int k = kBallot ? kb : __reduce_min_sync(gmask, next);
         if (k >= num_nodes) break;
         const float4 c = __ldg(a.com + k);
         const int4 w = __ldg(a.wnode + k);
-        bool open[T];
-        bool any_open = false;
-        bool descend = false;
-#pragma unroll
-        for (int i = 0; i < T; ++i) {
-            open[i] = false;
-            if (next[i] == k) {
-                const float dx = __fsub_rn(c.x, xi[i].x);
-                const float dy = __fsub_rn(c.y, xi[i].y);
-                const float dz = __fsub_rn(c.z, xi[i].z);
-                const float d2 = dist2(dx, dy, dz);
-                if (__int_as_float(w.w) < __fmul_rn(a.theta2, d2)) {
-                    add_term<kFast>(dx, dy, dz, d2, c.w, a.eps2, ax[i], ay[i], az[i]);
-                    if (kCount) ++pc[i];
-                    next[i] = w.x;
-                } else {
-                    open[i] = w.z != 0;
-                    next[i] = open[i] ? w.x : k + 1;
-                    descend |= !open[i];
-                }
+        bool open = false, descend = false;
+        if (next == k) {
+            const float dx = __fsub_rn(c.x, xi.x);
+            const float dy = __fsub_rn(c.y, xi.y);
+            const float dz = __fsub_rn(c.z, xi.z);
+            const float d2 = dist2(dx, dy, dz);
+            if (__int_as_float(w.w) < __fmul_rn(a.theta2, d2)) {
+                add_term<kFast>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
+                if (kCount) ++pc;
+                next = w.x;
+            } else {
+                open = w.z != 0;
+                next = open ? w.x : k + 1;
+                descend = !open;
             }
-            any_open |= open[i];
         }
         if (kBallot) kb = __any_sync(gmask, descend) ? k + 1 : w.x;
-        if (__any_sync(gmask, any_open)) {
+        if (__any_sync(gmask, open)) {
             const int first = w.y, count = w.z;
             if (first < 0 || first > a.n - count) {  // group-uniform consistency check
                 if (glane == 0) atomicOr(&a.P->status, kStatusInternal);
                 break;
             }
-#pragma unroll
-            for (int i = 0; i < T; ++i)
-                if (kCount && open[i])
-                    pp[i] += count - ((unsigned)(tgt[i] - first) < (unsigned)count ? 1u : 0u);
+            if (kCount && open) pp += count - ((unsigned)(tgt - first) < (unsigned)count ? 1u : 0u);
             for (int b = 0; b < count; b += G) {
                 const int chunk = min(G, count - b);
                 if (glane < chunk) stage[glane] = __ldg(a.ps + first + b + glane);
                 __syncwarp(gmask);
-#pragma unroll
-                for (int i = 0; i < T; ++i) {
-                    if (!open[i]) continue;
+                if (open) {
                     if (kSelfFree) {
 #pragma unroll 4
                         for (int j = 0; j < chunk; ++j)
-                            particle_term<kFast>(stage[j], xi[i], a.eps2, ax[i], ay[i], az[i]);
+                            particle_term<kFast>(stage[j], xi, a.eps2, ax, ay, az);
                     } else {
-                        const int self = tgt[i] - (first + b);
+                        const int self = tgt - (first + b);
                         for (int j = 0; j < chunk; ++j)
-                            if (j != self) particle_term<kFast>(stage[j], xi[i], a.eps2, ax[i], ay[i], az[i]);
+                            if (j != self) particle_term<kFast>(stage[j], xi, a.eps2, ax, ay, az);
                     }
                 }
                 __syncwarp(gmask);
@@ -275,9 +238,7 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
         }
     }
     if (steps > num_nodes && glane == 0) atomicOr(&a.P->status, kStatusWalkBound);
-#pragma unroll
-    for (int i = 0; i < T; ++i)  // every step visits the group's union
-        if (valid[i]) store_target<kCount>(a, tgt[i], ax[i], ay[i], az[i], pc[i], pp[i], steps);
+    if (valid) store_target<kCount>(a, tgt, ax, ay, az, pc, pp, steps);  // every step visits the union
 }
 
 template <int W, bool kCount, bool kBallot, bool kFast>
@@ -287,12 +248,156 @@ __global__ void __launch_bounds__(kThreads) k_walk_coherent(WalkArgs a)
     int num_nodes;
     bool self_free;
     if (!prologue<kFast>(a, num_nodes, self_free)) return;  // block-uniform
-    constexpr int G = Group<W>::G;
-    float4 *stage = &s_leaf[threadIdx.x >> 5][(threadIdx.x & 31) & ~(G - 1)];
+    float4 *stage = &s_leaf[threadIdx.x >> 5][(threadIdx.x & 31) & ~(W - 1)];
     if (self_free)
         coherent_walk<W, kCount, true, kBallot, kFast>(a, num_nodes, stage);
     else
         coherent_walk<W, kCount, false, kBallot, kFast>(a, num_nodes, stage);
+}
+
+// ---------------------------------------------------------------------------
+// Width 64: one warp, two targets per lane, in packed pairs. Blackwell issues
+// two binary32 operations of one thread in one instruction (__fadd2_rn,
+// __fmul2_rn, __ffma2_rn; each component is rounded exactly like its scalar
+// form), so a lane does both of its targets' acceptance tests and terms in
+// the issue slots of one. The warp still shares one node index, the minimum
+// over its 64 targets' wanted indices, and each target still follows its own
+// walk. To keep a pair in step, the cell term at node k is evaluated for both
+// targets of every lane, and a target that does not accept k (or is not at k)
+// adds it with a zero factor: fma(+0, dx, a) = a exactly for any finite dx (a
+// is never -0, see the file comment), so its sum is unchanged bit for bit.
+// Leaf particles are handled the same way for targets that did not open the
+// leaf. Every separation is finite because coordinates below 2^125 and node
+// centres of mass below 2^126 are checked before the walk runs.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
+
+template <bool kFast>
+__device__ __forceinline__ float2 inv_sqrt2(float2 x)
+{
+    if (kFast) return make_float2(rsqrtf(x.x), rsqrtf(x.y));
+    // rsqrt_newton componentwise; -h is formed as fl(-x/2), which equals
+    // -fl(x/2) bit for bit
+    const float2 nh = __fmul2_rn(splat(-0.5f), x);
+    float2 y = make_float2(__int_as_float(0x5f375a86 - (int)((unsigned)__float_as_int(x.x) >> 1)),
+                           __int_as_float(0x5f375a86 - (int)((unsigned)__float_as_int(x.y) >> 1)));
+#pragma unroll
+    for (int it = 0; it < 3; ++it) y = __fmul2_rn(y, __ffma2_rn(nh, __fmul2_rn(y, y), splat(1.5f)));
+    return y;
+}
+
+// Separations of a lane's two targets from one source (a cell's CoM or a
+// leaf particle), and their squared distances in the order of dist2.
+struct Sep2 {
+    float2 dx, dy, dz, d2;
+};
+
+__device__ __forceinline__ Sep2 separation2(float sx, float sy, float sz, float2 nx, float2 ny, float2 nz)
+{
+    Sep2 s;
+    s.dx = __fadd2_rn(splat(sx), nx);  // sx - x_i, formed as sx + (-x_i): the same rounding
+    s.dy = __fadd2_rn(splat(sy), ny);
+    s.dz = __fadd2_rn(splat(sz), nz);
+    s.d2 = __ffma2_rn(s.dz, s.dz, __ffma2_rn(s.dy, s.dy, __fmul2_rn(s.dx, s.dx)));
+    return s;
+}
+
+// add_term for both targets; a target with use == false adds a zero factor.
+template <bool kFast>
+__device__ __forceinline__ void add_term2(const Sep2 &s, float m, bool use0, bool use1, float2 eps2,
+                                          float2 &ax, float2 &ay, float2 &az)
+{
+    const float2 y = inv_sqrt2<kFast>(__fadd2_rn(s.d2, eps2));
+    const float2 fp = __fmul2_rn(__fmul2_rn(splat(m), y), __fmul2_rn(y, y));
+    const float2 f = make_float2(use0 ? fp.x : 0.0f, use1 ? fp.y : 0.0f);
+    ax = __ffma2_rn(f, s.dx, ax);
+    ay = __ffma2_rn(f, s.dy, ay);
+    az = __ffma2_rn(f, s.dz, az);
+}
+
+// Lane l of warp w holds sorted targets 64w + l and 64w + 32 + l.
+template <bool kCount, bool kSelfFree, bool kFast>
+__device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, float4 *stage)
+{
+    constexpr unsigned kFull = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const int base = ((blockIdx.x * kThreads + threadIdx.x) >> 5) * 64;
+    const int t0 = base + lane, t1 = base + 32 + lane;
+    const bool v0 = t0 < a.n, v1 = t1 < a.n;
+    const float4 p0 = v0 ? __ldg(a.ps + t0) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const float4 p1 = v1 ? __ldg(a.ps + t1) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    // negated positions: every separation is then one packed add
+    const float2 nx = make_float2(-p0.x, -p1.x), ny = make_float2(-p0.y, -p1.y),
+                 nz = make_float2(-p0.z, -p1.z);
+    const float2 theta2 = splat(a.theta2), eps2 = splat(a.eps2);
+    float2 ax = splat(0.0f), ay = splat(0.0f), az = splat(0.0f);
+    uint32_t pc0 = 0, pc1 = 0, pp0 = 0, pp1 = 0;
+    int next0 = v0 ? 0 : num_nodes, next1 = v1 ? 0 : num_nodes;
+    int steps = 0;
+    for (; steps <= num_nodes; ++steps) {
+        const int k = __reduce_min_sync(kFull, min(next0, next1));
+        if (k >= num_nodes) break;
+        const float4 c = __ldg(a.com + k);
+        const int4 w = __ldg(a.wnode + k);
+        const bool act0 = next0 == k, act1 = next1 == k;
+        const Sep2 s = separation2(c.x, c.y, c.z, nx, ny, nz);
+        const float2 lim = __fmul2_rn(theta2, s.d2);
+        const float s2 = __int_as_float(w.w);
+        const bool acc0 = act0 && s2 < lim.x, acc1 = act1 && s2 < lim.y;
+        // unconditional: nine steps in ten have an accepting target, and
+        // skipping the rest costs more in branching than it saves
+        add_term2<kFast>(s, c.w, acc0, acc1, eps2, ax, ay, az);
+        if (kCount) {
+            pc0 += acc0;
+            pc1 += acc1;
+        }
+        const bool leaf = w.z != 0;
+        const bool open0 = act0 && !acc0 && leaf, open1 = act1 && !acc1 && leaf;
+        if (act0) next0 = (acc0 || leaf) ? w.x : k + 1;
+        if (act1) next1 = (acc1 || leaf) ? w.x : k + 1;
+        if (__any_sync(kFull, open0 || open1)) {
+            const int first = w.y, count = w.z;
+            if (first < 0 || first > a.n - count) {  // warp-uniform consistency check
+                if (lane == 0) atomicOr(&a.P->status, kStatusInternal);
+                break;
+            }
+            if (kCount) {
+                pp0 += open0 ? count - ((unsigned)(t0 - first) < (unsigned)count ? 1u : 0u) : 0u;
+                pp1 += open1 ? count - ((unsigned)(t1 - first) < (unsigned)count ? 1u : 0u) : 0u;
+            }
+            for (int b = 0; b < count; b += 32) {
+                const int chunk = min(32, count - b);
+                if (lane < chunk) stage[lane] = __ldg(a.ps + first + b + lane);
+                __syncwarp();
+                const int self0 = t0 - (first + b), self1 = t1 - (first + b);
+#pragma unroll 4
+                for (int j = 0; j < chunk; ++j) {
+                    const float4 q = stage[j];
+                    const Sep2 sj = separation2(q.x, q.y, q.z, nx, ny, nz);
+                    add_term2<kFast>(sj, q.w, open0 && (kSelfFree || j != self0),
+                                     open1 && (kSelfFree || j != self1), eps2, ax, ay, az);
+                }
+                __syncwarp();
+            }
+        }
+    }
+    if (steps > num_nodes && lane == 0) atomicOr(&a.P->status, kStatusWalkBound);
+    if (v0) store_target<kCount>(a, t0, ax.x, ay.x, az.x, pc0, pp0, steps);
+    if (v1) store_target<kCount>(a, t1, ax.y, ay.y, az.y, pc1, pp1, steps);
+}
+
+template <bool kCount, bool kFast>
+__global__ void __launch_bounds__(kThreads) k_walk_paired(WalkArgs a)
+{
+    __shared__ float4 s_leaf[kWarpsPerBlock][32];
+    int num_nodes;
+    bool self_free;
+    if (!prologue<kFast>(a, num_nodes, self_free)) return;  // block-uniform
+    float4 *stage = s_leaf[threadIdx.x >> 5];
+    if (self_free)
+        paired_walk<kCount, true, kFast>(a, num_nodes, stage);
+    else
+        paired_walk<kCount, false, kFast>(a, num_nodes, stage);
 }
 
 // The scheme the pages reject, kept as a measured contrast (ADR-0029,
@@ -427,19 +532,24 @@ __global__ void __launch_bounds__(kThreads) k_walk_independent(WalkArgs a)
 template <bool kFast>
 void launch_kernels(int traversal, bool count, unsigned grid, const WalkArgs &a, cudaStream_t st)
 {
-    // coherent groups of W targets: kThreads lanes cover kThreads * T targets
     auto coherent = [&](auto wtag) {
         constexpr int W = decltype(wtag)::value;
-        const unsigned g = ceil_div(a.n, (int64_t)kThreads * Group<W>::T);
         if (count)
-            k_walk_coherent<W, true, false, kFast><<<g, kThreads, 0, st>>>(a);
+            k_walk_coherent<W, true, false, kFast><<<grid, kThreads, 0, st>>>(a);
         else
-            k_walk_coherent<W, false, false, kFast><<<g, kThreads, 0, st>>>(a);
+            k_walk_coherent<W, false, false, kFast><<<grid, kThreads, 0, st>>>(a);
     };
     switch (traversal) {
     case 1: coherent(std::integral_constant<int, 32>{}); break;
     case 2: coherent(std::integral_constant<int, 16>{}); break;
-    case 3: coherent(std::integral_constant<int, 64>{}); break;
+    case 3: {
+        const unsigned g = ceil_div(a.n, (int64_t)kThreads * 2);  // 64 targets per warp
+        if (count)
+            k_walk_paired<true, kFast><<<g, kThreads, 0, st>>>(a);
+        else
+            k_walk_paired<false, kFast><<<g, kThreads, 0, st>>>(a);
+        break;
+    }
     case 4:
         if (count)
             k_walk_together<true, kFast><<<grid, kThreads, 0, st>>>(a);
