@@ -5,7 +5,8 @@ radix sort, gather, octree build, moments, coherent walk, scatter) with the
 inputs already resident in device memory. Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--traversal coherent|independent] [--impl ours|reference]
+                    [--traversal coherent64|coherent|independent|...] [--term fast|exact]
+                    [--impl ours|reference]
 
 --impl reference times the CPU oracle (the plain C restatement of the
 method) on this host's cores instead, on a bounded sample of the same
@@ -44,16 +45,18 @@ def parse():
     p.add_argument("--steps", type=int, default=11)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--workload", default="plummer_1048576")
-    p.add_argument("--traversal", default="coherent",
+    p.add_argument("--traversal", default="coherent64",
                    choices=["coherent", "coherent16", "coherent64", "ballot", "together",
                             "independent"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=8.0,
                    help="target wall time of the CPU-oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--fast-term", action="store_true",
-                   help="time the approximate inverse square root (ORRERY_FAST_TERM) instead of "
-                        "the bit-reproducible term")
+    p.add_argument("--term", default="fast", choices=["fast", "exact"],
+                   help="fast: the hardware approximate inverse square root (ORRERY_FAST_TERM; "
+                        "within 1e-5 of the oracle, counts identical); exact: the "
+                        "bit-reproducible Newton term (the oracle's bits). The other one is "
+                        "timed too and reported beside the headline")
     p.add_argument("--scaling", action="store_true",
                    help="instead of the benchmark line, the pages' scaling study: one JSON "
                         "line per N from 1024 to 16M particles")
@@ -109,7 +112,8 @@ def run_scaling(args) -> None:
         for it in range(args.warmup + args.steps):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            tt.bh_forces(pos, mass, 0.5, 0.05, 32, args.traversal, out=(acc, inter, vis))
+            tt.bh_forces(pos, mass, 0.5, 0.05, 32, args.traversal, out=(acc, inter, vis),
+                         fast_term=args.term == "fast")
             b.record(stream)
             torch.cuda.synchronize(dev)
             if it >= args.warmup:
@@ -124,7 +128,8 @@ def run_scaling(args) -> None:
                "cells_per_particle": float(inter[:, 0].double().mean()),
                "interactions_per_particle": float(inter.double().sum(1).mean()),
                "visits_per_particle": float(vis.double().mean()),
-               "nodes": tm["num_nodes"], "depth": tm["depth"], "traversal": args.traversal}
+               "nodes": tm["num_nodes"], "depth": tm["depth"], "traversal": args.traversal,
+               "term": args.term}
         prev = (n, t)
         print(json.dumps(row), flush=True)
         del pos, mass, acc, inter, vis
@@ -162,13 +167,14 @@ def run_crossover(args) -> None:
         pos_np, mass_np = plummer(n)
         pos = torch.from_numpy(pos_np).to(dev)
         mass = torch.from_numpy(mass_np).to(dev)
-        t_tree = timed(lambda: tt.bh_forces(pos, mass, 0.5, 0.05, 32, args.traversal))
+        t_tree = timed(lambda: tt.bh_forces(pos, mass, 0.5, 0.05, 32, args.traversal,
+                                            fast_term=args.term == "fast"))
         walk = tt.last_timings()["walk_ms"]
         t_direct = timed(lambda: tt.direct_forces(pos, mass, 0.05))
         print(json.dumps({"n": n, "tree_ms": t_tree, "tree_walk_ms": walk, "direct_ms": t_direct,
                           "tree_speedup_vs_direct": t_direct / t_tree,
                           "direct_pairs_per_s": n * (n - 1) / (t_direct / 1000.0),
-                          "traversal": args.traversal}), flush=True)
+                          "traversal": args.traversal, "term": args.term}), flush=True)
 
 
 def measured_peaks() -> dict:
@@ -179,11 +185,21 @@ def measured_peaks() -> dict:
         return {}
 
 
-def profile_traffic(kernel_src: str) -> float | None:
+# the walk kernel each traversal launches, and the ncu summary holding its
+# full-size DRAM traffic
+WALK_KERNELS = {"coherent": "k_walk_coherent", "coherent16": "k_walk_coherent",
+                "ballot": "k_walk_coherent", "coherent64": "k_walk_paired",
+                "together": "k_walk_together", "independent": "k_walk_independent"}
+TRAFFIC_PROFILES = {("k_walk_paired", True): "walk_paired_fast_plummer_1m.md",
+                    ("k_walk_coherent", False): "walk_coherent_plummer_1m.md"}
+
+
+def profile_traffic(kernel_src: str, kernel: str, fast: bool) -> float | None:
     """Per-launch DRAM bytes of the walk kernel from the committed ncu summary,
     only while the kernel source is the one that was profiled."""
-    path = os.path.join(ROOT, "profiles", "walk_coherent_plummer_1m.md")
-    if not os.path.exists(path):
+    name = TRAFFIC_PROFILES.get((kernel, fast))
+    path = os.path.join(ROOT, "profiles", name) if name else ""
+    if not name or not os.path.exists(path):
         return None
     sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
     found_sha, traffic = None, None
@@ -356,14 +372,23 @@ def main():
     visits = torch.empty(n, dtype=torch.int32, device=device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
-    call = lambda trav: tt.bh_forces(pos, mass, params["theta"], params["eps"], params["leaf_cap"],
-                                     trav, out=(acc, inter, visits), fast_term=args.fast_term)
+    fast = args.term == "fast"
+    call = lambda trav, fast_term=fast: tt.bh_forces(
+        pos, mass, params["theta"], params["eps"], params["leaf_cap"], trav,
+        out=(acc, inter, visits), fast_term=fast_term)
 
-    # untimed: the comparison traversal (its visits give the redundancy ratio)
+    # untimed: the comparison traversals (the independent walk's visits give
+    # the redundancy ratio; width 32 is the pages' coherent group)
+    comparison = {}
+    for trav in ("independent", "coherent", "coherent64"):
+        if trav == args.traversal:
+            continue
+        for _ in range(2):
+            call(trav)
+        comparison[trav] = {"walk_ms": tt.last_timings()["walk_ms"],
+                            "visits_per_particle": visits.double().mean().item()}
     other = "independent" if args.traversal != "independent" else "coherent"
-    call(other)
-    t_other = tt.last_timings()
-    vis_other = visits.double().mean().item()
+    vis_other = comparison[other]["visits_per_particle"]
     for _ in range(args.warmup):
         call(args.traversal)
     torch.cuda.synchronize(device)
@@ -395,6 +420,19 @@ def main():
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms_per_step, value = replica_throughput(sum(step_ms), interactions, args.steps, dist, device)
 
+    # the other term, timed the same way (reported beside the headline)
+    for _ in range(3):
+        call(args.traversal, not fast)
+    other_ms, other_walk = [], []
+    for s in range(args.steps):
+        flush.zero_()
+        ev[s][0].record(stream)
+        call(args.traversal, not fast)
+        ev[s][1].record(stream)
+        other_walk.append(tt.last_timings()["walk_ms"])
+    torch.cuda.synchronize(device)
+    other_ms = [a.elapsed_time(b) for a, b in ev]
+
     def mean(key):
         return statistics.fmean(p[key] for p in phases)
 
@@ -417,14 +455,14 @@ def main():
              torch.empty(n, dtype=torch.int32).pin_memory())
     for _ in range(2):
         tt.bh_forces_host(h_pos, h_mass, params["theta"], params["eps"], params["leaf_cap"],
-                          args.traversal, out=h_out, device=device)
+                          args.traversal, out=h_out, device=device, fast_term=fast)
     e2e_ms = []
     for _ in range(args.steps):
         flush.zero_()
         torch.cuda.synchronize(device)
         t1 = time.perf_counter()
         tt.bh_forces_host(h_pos, h_mass, params["theta"], params["eps"], params["leaf_cap"],
-                          args.traversal, out=h_out, device=device)
+                          args.traversal, out=h_out, device=device, fast_term=fast)
         e2e_ms.append(1000.0 * (time.perf_counter() - t1))
     e2e_host = tt.last_timings()
     if dist is not None:
@@ -436,7 +474,8 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         cb = cpu_baseline(pos_np, mass_np, params, args.cpu_seconds)
     walk_src = os.path.join(ROOT, "tree_traversal_gb300", "csrc", "bh_walk.cu")
-    traffic = profile_traffic(walk_src)
+    kernel = WALK_KERNELS[args.traversal]
+    traffic = profile_traffic(walk_src, kernel, fast)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -444,14 +483,13 @@ def main():
         "config": {"workload": args.workload, "n": n, "theta": params["theta"],
                    "eps": params["eps"], "leaf_cap": params["leaf_cap"],
                    "traversal": args.traversal, "parallelism": "replicas" if world > 1 else "1gpu",
-                   "term": "fast (approximate inverse root)" if args.fast_term
-                   else "bit-reproducible (Newton inverse root)",
+                   "term": "fast: hardware approximate inverse root, within 1e-5 of the oracle"
+                   if fast else "exact: Newton inverse root, the oracle's bits",
                    "l2": "flushed between steps (256 MiB write outside the step events)"},
         "gpu_launches": int(launches),
         "clocks": {"sm_mhz": csum["sm_mhz"], "sm_max_mhz": csum["sm_max_mhz"],
                    "reasons": csum["reasons"]},
-        "roofline": {"bound": "alu", "kernel": "k_walk_independent"
-                     if args.traversal == "independent" else "k_walk_coherent",
+        "roofline": {"bound": "alu", "kernel": kernel,
                      "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / peak_tflops, "traffic": traffic,
                      "peak_basis": "%d SMs x %d FP32 lanes x 2 flop x %.0f MHz (max SM clock of "
@@ -479,7 +517,10 @@ def main():
                          "visits": vis_mean, "visits_" + other: vis_other,
                          "redundancy": (vis_mean / vis_other) if args.traversal != "independent"
                          else (vis_other / vis_mean)},
-        "walk_ms_" + other: t_other["walk_ms"],
+        ("exact_term" if fast else "fast_term"): {
+            "ms_per_step": statistics.fmean(other_ms), "walk_ms": statistics.fmean(other_walk),
+            "value": interactions / (statistics.fmean(other_ms) / 1000.0)},
+        "comparison_traversals": comparison,
     }
     print(json.dumps(line), flush=True)
 

@@ -79,20 +79,23 @@ typedef enum {
     ORRERY_INDEPENDENT = 0,       /* one thread per target, each on its own node index */
     ORRERY_COHERENT = 1,          /* 32 targets (one warp) share a node index */
     ORRERY_COHERENT_16 = 2,       /* 16 targets (half a warp) share a node index */
-    ORRERY_COHERENT_64 = 3,       /* 64 targets (one warp, two per lane) share a node index */
+    ORRERY_COHERENT_64 = 3,       /* 64 targets (one warp, two per lane, packed float2
+                                     arithmetic) share a node index: the fastest */
     ORRERY_DESCEND_TOGETHER = 4,  /* comparison only: group-dependent answer */
     ORRERY_COHERENT_BALLOT = 5    /* as ORRERY_COHERENT, next node by vote + escape
                                      instead of a minimum reduction (same visits) */
 } orrery_traversal;
 
 /* Flag ORed into the traversal argument: the force term's inverse square
- * root uses the hardware approximation (rsqrtf) instead of the fixed Newton
- * sequence. The walk is then ~16 % faster, acceptance decisions, counts and
- * visits are unchanged, and accelerations agree with the exact path to
- * rounding instead of bit for bit (at most 4.4e-6 relative on the Plummer
- * and two-sphere configurations at 1M-2M particles; the tests bound it by
- * 1e-5). Without the flag results are reproducible bit for bit on any
- * IEEE-754 CPU. */
+ * root uses the hardware approximation (rsqrt.approx) instead of the fixed
+ * Newton sequence. The width-64 walk is then ~15 % faster; acceptance
+ * decisions, counts and visits are unchanged, and accelerations agree with
+ * the exact path to rounding instead of bit for bit: at most 4.4e-6 relative
+ * on the Plummer and two-sphere workloads (softening 0.05, 1M-2M particles),
+ * bounded by 1e-5 in the tests at softening 0.05 and above. Without softening
+ * the per-term error can be multiplied by cancellation between close pairs
+ * (1.6e-5 seen at eps = 1e-20), so the exact term is the one to use there.
+ * Without the flag results are reproducible bit for bit on any IEEE-754 CPU. */
 #define ORRERY_FAST_TERM 0x100
 
 /* Where the last evaluation spent its time ("sycl_tree_solver.hpp",

@@ -168,6 +168,17 @@ def test_forces_softening_sweep(tt, name, eps):
         assert np.array_equal(g.view(np.uint32), r_acc.view(np.uint32))
         g_inter = u32(inter)[T.perm]
         assert np.array_equal(g_inter[:, 0], r_pc) and np.array_equal(g_inter[:, 1], r_pp)
+        if eps > 0:
+            # the fast term: the full hardware root when eps^2 is below FLT_MIN,
+            # the flushing one above. The 1e-5 bar holds at the softening of
+            # the workloads (0.05) and above; without softening (eps = 1e-20)
+            # close pairs make terms that nearly cancel, which multiplies the
+            # root's few-ulp error (1.6e-5 seen here), so that case is held
+            # to 1e-4
+            f, fi, _ = tt.bh_forces(dev(pos), dev(mass), 0.5, eps, cap, traversal, fast_term=True)
+            tol = REL_TOL if eps >= 0.05 else 1e-4
+            assert oracle.relative_error(f.cpu().numpy()[T.perm], r_acc).max() <= tol
+            assert torch.equal(fi, inter)
 
 
 def test_coincident_points_without_softening(tt):
@@ -322,6 +333,14 @@ def check_full_size(tt, pos, mass, thetas, cap=32):
         t64 = np.concatenate([np.arange(64 * g, min(T.n, 64 * g + 64)) for g in g64])
         assert np.array_equal(u32(v64)[T.perm[t64]],
                               np.repeat(u64, [min(64, T.n - 64 * g) for g in g64]))
+        # the fast term on the width-64 walk: every target within the
+        # tolerance of the exact sums, every count identical
+        f64, j64, w64 = tt.bh_forces(p, m, theta, EPS, cap, "coherent64", fast_term=True)
+        assert torch.equal(j64, inter) and torch.equal(w64, v64)
+        ref = acc.double()
+        ok = ref.norm(dim=1) > 0
+        rel = (f64.double() - ref).norm(dim=1)[ok] / ref.norm(dim=1)[ok]
+        assert float(rel.max()) <= REL_TOL
 
 
 def test_full_size_plummer_1m(tt):
@@ -456,12 +475,18 @@ def test_fast_term_within_tolerance(tt, name, traversal):
 def test_fast_term_full_size_all_targets(tt):
     pos, mass = plummer(1048576, PAGES_SEED)
     T = oracle.Tree(pos, mass, 32)
-    acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), 0.5, EPS, 32, "coherent", fast_term=True)
     r_acc, r_pc, r_pp, _ = T.walk(0.5, EPS, threads=oracle.default_threads())
-    g = acc.cpu().numpy()[T.perm]
-    assert oracle.relative_error(g, r_acc).max() <= REL_TOL
-    gi = u32(inter)[T.perm]
-    assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)
+    for traversal in ("coherent64", "coherent"):
+        acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), 0.5, EPS, 32, traversal, fast_term=True)
+        g = acc.cpu().numpy()[T.perm]
+        assert oracle.relative_error(g, r_acc).max() <= REL_TOL
+        gi = u32(inter)[T.perm]
+        assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)
+    # the host entry point with the fast term gives the same bits as the device one
+    h = tt.bh_forces_host(pos, mass, 0.5, EPS, 32, "coherent64", fast_term=True)
+    d = tt.bh_forces(dev(pos), dev(mass), 0.5, EPS, 32, "coherent64", fast_term=True)
+    assert np.array_equal(h[0].view(np.uint32), d[0].cpu().numpy().view(np.uint32))
+    assert np.array_equal(h[1], u32(d[1]))
 
 
 # ---------------------------------------------------------------------------

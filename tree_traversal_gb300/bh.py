@@ -82,10 +82,12 @@ def bh_forces(pos: torch.Tensor, mass: torch.Tensor, theta: float = 0.5, eps: fl
 
 
 def bh_forces_host(pos: np.ndarray, mass: np.ndarray, theta: float = 0.5, eps: float = 0.05,
-                   leaf_cap: int = 32, traversal="coherent", out=None, device=None):
+                   leaf_cap: int = 32, traversal="coherent", out=None, device=None,
+                   fast_term: bool = False):
     """The same evaluation from host arrays (numpy or CPU tensors, page-locked
     for the fastest copies) to host arrays; the copies run inside the call.
-    ``out`` = (acc [n,3] f32, interactions [n,2] u32 or None, visits [n] u32 or None)."""
+    ``out`` = (acc [n,3] f32, interactions [n,2] u32 or None, visits [n] u32 or None);
+    ``fast_term`` as for bh_forces."""
     def host_ptr(a, shape, dtype):
         if isinstance(a, torch.Tensor):
             if a.is_cuda or not a.is_contiguous() or tuple(a.shape) != shape or \
@@ -104,7 +106,8 @@ def bh_forces_host(pos: np.ndarray, mass: np.ndarray, theta: float = 0.5, eps: f
     with torch.cuda.device(dev):
         rc = _lib.load().orrery_bh_forces_host(
             host_ptr(pos, (n, 3), np.float32), host_ptr(mass, (n,), np.float32), n, float(theta),
-            float(eps), int(leaf_cap), _traversal(traversal), host_ptr(acc, (n, 3), np.float32),
+            float(eps), int(leaf_cap), _traversal(traversal) | (_lib.FAST_TERM if fast_term else 0),
+            host_ptr(acc, (n, 3), np.float32),
             None if inter is None else host_ptr(inter, (n, 2), np.uint32),
             None if visits is None else host_ptr(visits, (n,), np.uint32), _stream_handle(dev))
     if rc != _lib.OK:

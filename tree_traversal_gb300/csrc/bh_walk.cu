@@ -36,9 +36,13 @@
 // Summing it instead changes nothing, bit for bit, whenever its force factor
 // is finite: dx = dy = dz = +0, so fma(f, +0, a) = a (a is never -0: it
 // starts at +0 and round-to-nearest never produces -0 from a sum of unlike
-// signs). The factor is finite iff eps > 0 and (m_max y)(y y) does not
-// overflow for y = rsqrt(eps^2); the kernels test that once per block and
-// drop the per-particle self comparison when it holds.
+// signs). The kernels test once per block that eps^2 is a normal number and
+// that twice the largest particle factor, (m_max y)(y y) at y = rsqrt(eps^2),
+// is finite; then every factor is finite (r2 >= eps^2 and the roots are within
+// a few ulp of monotone), every r2 is normal (so the fast term may use the
+// flush-to-zero hardware root), and the per-particle self comparison is
+// dropped.
+#include <cfloat>
 #include <type_traits>
 
 #include "bh_common.cuh"
@@ -99,21 +103,32 @@ __device__ __forceinline__ float rsqrt_newton(float x)
     return y;
 }
 
-// kFast selects the hardware approximate inverse square root (rsqrtf, a few
-// ulp) in place of the Newton sequence: faster, no longer reproducible bit for
-// bit on a CPU (the caller opts in with ORRERY_FAST_TERM).
-template <bool kFast>
-__device__ __forceinline__ float inv_sqrt(float x)
+// The hardware approximate inverse square root with subnormal inputs flushed:
+// the same value as rsqrtf for every normal input, without rsqrtf's extra
+// handling of subnormal ones.
+__device__ __forceinline__ float rsqrt_ftz(float x)
 {
-    return kFast ? rsqrtf(x) : rsqrt_newton(x);
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-template <bool kFast>
+// kFast selects the hardware approximate inverse square root (a few ulp) in
+// place of the Newton sequence: faster, no longer reproducible bit for bit on
+// a CPU (the caller opts in with ORRERY_FAST_TERM). kNormal: the argument is
+// known to be a normal number (every r2 >= eps^2 >= FLT_MIN).
+template <bool kFast, bool kNormal = false>
+__device__ __forceinline__ float inv_sqrt(float x)
+{
+    return kFast ? (kNormal ? rsqrt_ftz(x) : rsqrtf(x)) : rsqrt_newton(x);
+}
+
+template <bool kFast, bool kNormal = false>
 __device__ __forceinline__ void add_term(float dx, float dy, float dz, float d2, float m,
                                          float eps2, float &ax, float &ay, float &az)
 {
     const float r2 = __fadd_rn(d2, eps2);
-    const float y = inv_sqrt<kFast>(r2);
+    const float y = inv_sqrt<kFast, kNormal>(r2);
     const float f = __fmul_rn(__fmul_rn(m, y), __fmul_rn(y, y));
     ax = __fmaf_rn(f, dx, ax);
     ay = __fmaf_rn(f, dy, ay);
@@ -125,14 +140,14 @@ __device__ __forceinline__ float dist2(float dx, float dy, float dz)
     return __fmaf_rn(dz, dz, __fmaf_rn(dy, dy, __fmul_rn(dx, dx)));
 }
 
-template <bool kFast>
+template <bool kFast, bool kNormal = false>
 __device__ __forceinline__ void particle_term(const float4 &p, const float4 &xi, float eps2,
                                               float &ax, float &ay, float &az)
 {
     const float dx = __fsub_rn(p.x, xi.x);
     const float dy = __fsub_rn(p.y, xi.y);
     const float dz = __fsub_rn(p.z, xi.z);
-    add_term<kFast>(dx, dy, dz, dist2(dx, dy, dz), p.w, eps2, ax, ay, az);
+    add_term<kFast, kNormal>(dx, dy, dz, dist2(dx, dy, dz), p.w, eps2, ax, ay, az);
 }
 
 // Block prologue shared by both kernels: status, node count and whether the
@@ -145,11 +160,11 @@ __device__ __forceinline__ bool prologue(const WalkArgs &a, int &num_nodes, bool
         const DeviceParams *P = a.P;
         s_state[0] = P->status;
         s_state[1] = P->num_nodes;
-        bool ok = a.eps2 > 0.0f;
+        bool ok = a.eps2 >= FLT_MIN;
         if (ok) {
             const float y = inv_sqrt<kFast>(a.eps2);
             const float f = __fmul_rn(__fmul_rn(P->mmax, y), __fmul_rn(y, y));
-            ok = isfinite(f);
+            ok = isfinite(__fmul_rn(f, 2.0f));
         }
         s_state[2] = ok ? 1 : 0;
     }
@@ -201,7 +216,7 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
             const float dz = __fsub_rn(c.z, xi.z);
             const float d2 = dist2(dx, dy, dz);
             if (__int_as_float(w.w) < __fmul_rn(a.theta2, d2)) {
-                add_term<kFast>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
+                add_term<kFast, kSelfFree>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
                 if (kCount) ++pc;
                 next = w.x;
             } else {
@@ -226,11 +241,11 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
                     if (kSelfFree) {
 #pragma unroll 4
                         for (int j = 0; j < chunk; ++j)
-                            particle_term<kFast>(stage[j], xi, a.eps2, ax, ay, az);
+                            particle_term<kFast, kSelfFree>(stage[j], xi, a.eps2, ax, ay, az);
                     } else {
                         const int self = tgt - (first + b);
                         for (int j = 0; j < chunk; ++j)
-                            if (j != self) particle_term<kFast>(stage[j], xi, a.eps2, ax, ay, az);
+                            if (j != self) particle_term<kFast, kSelfFree>(stage[j], xi, a.eps2, ax, ay, az);
                     }
                 }
                 __syncwarp(gmask);
@@ -272,10 +287,10 @@ __global__ void __launch_bounds__(kThreads) k_walk_coherent(WalkArgs a)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
 
-template <bool kFast>
+template <bool kFast, bool kNormal = false>
 __device__ __forceinline__ float2 inv_sqrt2(float2 x)
 {
-    if (kFast) return make_float2(rsqrtf(x.x), rsqrtf(x.y));
+    if (kFast) return make_float2(inv_sqrt<true, kNormal>(x.x), inv_sqrt<true, kNormal>(x.y));
     // rsqrt_newton componentwise; -h is formed as fl(-x/2), which equals
     // -fl(x/2) bit for bit
     const float2 nh = __fmul2_rn(splat(-0.5f), x);
@@ -303,11 +318,11 @@ __device__ __forceinline__ Sep2 separation2(float sx, float sy, float sz, float2
 }
 
 // add_term for both targets; a target with use == false adds a zero factor.
-template <bool kFast>
+template <bool kFast, bool kNormal = false>
 __device__ __forceinline__ void add_term2(const Sep2 &s, float m, bool use0, bool use1, float2 eps2,
                                           float2 &ax, float2 &ay, float2 &az)
 {
-    const float2 y = inv_sqrt2<kFast>(__fadd2_rn(s.d2, eps2));
+    const float2 y = inv_sqrt2<kFast, kNormal>(__fadd2_rn(s.d2, eps2));
     const float2 fp = __fmul2_rn(__fmul2_rn(splat(m), y), __fmul2_rn(y, y));
     const float2 f = make_float2(use0 ? fp.x : 0.0f, use1 ? fp.y : 0.0f);
     ax = __ffma2_rn(f, s.dx, ax);
@@ -346,7 +361,7 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
         const bool acc0 = act0 && s2 < lim.x, acc1 = act1 && s2 < lim.y;
         // unconditional: nine steps in ten have an accepting target, and
         // skipping the rest costs more in branching than it saves
-        add_term2<kFast>(s, c.w, acc0, acc1, eps2, ax, ay, az);
+        add_term2<kFast, kSelfFree>(s, c.w, acc0, acc1, eps2, ax, ay, az);
         if (kCount) {
             pc0 += acc0;
             pc1 += acc1;
@@ -374,7 +389,7 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
                 for (int j = 0; j < chunk; ++j) {
                     const float4 q = stage[j];
                     const Sep2 sj = separation2(q.x, q.y, q.z, nx, ny, nz);
-                    add_term2<kFast>(sj, q.w, open0 && (kSelfFree || j != self0),
+                    add_term2<kFast, kSelfFree>(sj, q.w, open0 && (kSelfFree || j != self0),
                                      open1 && (kSelfFree || j != self1), eps2, ax, ay, az);
                 }
                 __syncwarp();
@@ -427,7 +442,7 @@ __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, 
         const bool accept = __int_as_float(w.w) < __fmul_rn(a.theta2, d2);
         if (__all_sync(0xffffffffu, accept || !valid)) {
             if (valid) {
-                add_term<kFast>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
+                add_term<kFast, kSelfFree>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
                 if (kCount) ++pc;
             }
             k = w.x;
@@ -447,11 +462,11 @@ __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, 
                     if (kSelfFree) {
 #pragma unroll 4
                         for (int j = 0; j < chunk; ++j)
-                            particle_term<kFast>(stage[j], xi, a.eps2, ax, ay, az);
+                            particle_term<kFast, kSelfFree>(stage[j], xi, a.eps2, ax, ay, az);
                     } else {
                         const int self = t - (first + b);
                         for (int j = 0; j < chunk; ++j)
-                            if (j != self) particle_term<kFast>(stage[j], xi, a.eps2, ax, ay, az);
+                            if (j != self) particle_term<kFast, kSelfFree>(stage[j], xi, a.eps2, ax, ay, az);
                     }
                 }
                 __syncwarp();
@@ -496,7 +511,7 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
         const float dz = __fsub_rn(c.z, xi.z);
         const float d2 = dist2(dx, dy, dz);
         if (__int_as_float(w.w) < __fmul_rn(a.theta2, d2)) {
-            add_term<kFast>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
+            add_term<kFast, kSelfFree>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
             if (kCount) ++pc;
             k = w.x;
         } else if (w.z != 0) {
@@ -507,7 +522,7 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
             }
             if (kCount) pp += count - ((unsigned)(t - first) < (unsigned)count ? 1u : 0u);
             for (int j = first; j < first + count; ++j)
-                if (kSelfFree || j != t) particle_term<kFast>(__ldg(a.ps + j), xi, a.eps2, ax, ay, az);
+                if (kSelfFree || j != t) particle_term<kFast, kSelfFree>(__ldg(a.ps + j), xi, a.eps2, ax, ay, az);
             k = w.x;
         } else {
             k = k + 1;
