@@ -363,7 +363,7 @@ def test_full_size_two_spheres_theta_sweep(tt):
 # ---------------------------------------------------------------------------
 # direct summation (the pages' comparison solver)
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("n", [1, 2, 33, 255, 256, 257, 1000, 4097, 20000])
+@pytest.mark.parametrize("n", [1, 2, 33, 255, 256, 257, 511, 512, 513, 1000, 1025, 4097, 20000])
 def test_direct_bit_exact(tt, n):
     pos, mass = plummer(n, 1000 + n)
     acc = tt.direct_forces(dev(pos), dev(mass), EPS)
@@ -382,6 +382,18 @@ def test_direct_coincident_and_nonfinite(tt):
         tt.direct_forces(dev(p), dev(mass), EPS)
     assert e.value.status == -2
     assert tt.direct_forces(torch.zeros((0, 3), device="cuda"), torch.zeros(0, device="cuda")).shape == (0, 3)
+    # no softening: the self pair's factor is not finite, the select keeps it
+    # out; coincident distinct points give NaN on both sides
+    for eps in (0.0, 1e-20):
+        g = tt.direct_forces(dev(pos), dev(mass), eps).cpu().numpy()
+        r = oracle.direct_f32(pos, mass, eps)
+        assert np.array_equal(np.isnan(g), np.isnan(r))
+        ok = ~np.isnan(r)
+        assert np.array_equal(g[ok].view(np.uint32), r[ok].view(np.uint32))
+    q, mq = plummer(700, 77)
+    for eps in (0.0, 1e-20):
+        assert np.array_equal(tt.direct_forces(dev(q), dev(mq), eps).cpu().numpy().view(np.uint32),
+                              oracle.direct_f32(q, mq, eps).view(np.uint32))
 
 
 # ---------------------------------------------------------------------------
