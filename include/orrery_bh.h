@@ -144,6 +144,33 @@ int orrery_bh_forces(const float *pos_d, const float *mass_d, int64_t n, float t
                      uint32_t *visits_d, void *stream);
 
 /*
+ * orrery_bh_forces for a slice of the targets: the tree is built over all n
+ * particles (every particle is a source), and only the targets at SORTED
+ * positions [begin, end) are walked. Targets are independent once the tree
+ * exists ("sycl_tree_solver.hpp", "What is not given up": each target is
+ * summed over its own walk), so disjoint slices that cover [0, n) give,
+ * together, exactly the full evaluation: the unit a caller shards across
+ * devices or streams. Sorted positions are the Morton order of the particles
+ * (the permutation orrery_bh_tree returns); callers need not know it, only
+ * that equal slices of [0, n) partition the targets.
+ *   begin, end   0 <= begin <= end <= n, else ORRERY_EINVAL; begin == end
+ *                builds the tree and walks nothing
+ *   acc_d, interactions_d, visits_d  as in orrery_bh_forces, but only the
+ *                slice's targets are written (at their caller-order
+ *                positions); every other entry is left as it was
+ * Accelerations and interaction counts equal those of the full evaluation
+ * for every slice. Visit counts of a coherent traversal equal them when
+ * begin and end are multiples of the group width (end may also be n);
+ * otherwise the groups are formed from begin onward, so each count is the
+ * union over other neighbours (never below the target's own walk). The
+ * descend-together traversal's sums depend on the groups too.
+ */
+int orrery_bh_forces_range(const float *pos_d, const float *mass_d, int64_t n, float theta,
+                           float eps, int32_t leaf_cap, int32_t traversal, int64_t begin,
+                           int64_t end, float *acc_d, uint32_t *interactions_d, uint32_t *visits_d,
+                           void *stream);
+
+/*
  * The same evaluation from and to HOST memory (page-locked memory gives the
  * fastest copies; pageable memory works). The copies run on `stream` inside
  * the call; pos, mass and acc are required, interactions and visits may be

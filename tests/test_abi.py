@@ -95,6 +95,36 @@ def test_argument_checks_answer_on_the_host(lib):
     assert lib.orrery_bh_tree(P, P, 0, 32, P, P, P, P, P, 0, ctypes.byref(nn), P) == L.OK
     assert nn.value == 0
     assert lib.orrery_bh_tree(dummy, dummy, 10, 32, P, P, P, P, P, 0, None, P) == L.EINVAL
+    # the target-slice entry: the same checks, plus 0 <= begin <= end <= n
+    r = lib.orrery_bh_forces_range
+    assert r(dummy, dummy, 10, 0.5, 0.05, 32, 3, -1, 5, dummy, P, P, P) == L.EINVAL
+    assert r(dummy, dummy, 10, 0.5, 0.05, 32, 3, 6, 5, dummy, P, P, P) == L.EINVAL
+    assert r(dummy, dummy, 10, 0.5, 0.05, 32, 3, 0, 11, dummy, P, P, P) == L.EINVAL
+    assert r(dummy, dummy, 10, -0.5, 0.05, 32, 3, 0, 10, dummy, P, P, P) == L.EINVAL
+    assert r(dummy, dummy, 10, 0.5, 0.05, 32, 9, 0, 10, dummy, P, P, P) == L.EINVAL
+    assert r(P, dummy, 10, 0.5, 0.05, 32, 3, 0, 10, dummy, P, P, P) == L.EINVAL
+    assert r(dummy, dummy, 10, 0.5, 0.05, 32, 3, 0, 10, P, P, P, P) == L.EINVAL
+    assert r(dummy, dummy, 1 << 30, 0.5, 0.05, 1, 3, 0, 64, dummy, P, P, P) == L.ERANGE
+    assert r(P, P, 0, 0.5, 0.05, 32, 3, 0, 0, P, P, P, P) == L.OK
+
+
+def test_shard_tiles_the_targets():
+    import tree_traversal_gb300 as tt
+
+    for n in (0, 1, 63, 64, 65, 1000, 1048576, 1048577):
+        for world in (1, 2, 3, 4, 7, 8):
+            for align in (1, 32, 64):
+                cuts = [tt.shard(n, r, world, align) for r in range(world)]
+                assert cuts[0][0] == 0 and cuts[-1][1] == n
+                for (b0, e0), (b1, e1) in zip(cuts, cuts[1:]):
+                    assert e0 == b1
+                for b, e in cuts:
+                    assert 0 <= b <= e <= n
+                    assert b % align == 0 and (e % align == 0 or e == n)
+                sizes = [e - b for b, e in cuts]
+                assert max(sizes) - min(sizes) <= align
+    with pytest.raises(ValueError):
+        tt.shard(10, 2, 2)
 
 
 def test_node_bound(lib):

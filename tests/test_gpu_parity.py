@@ -543,3 +543,71 @@ def test_random_configurations_bit_exact(tt, seed):
     width = {"independent": 1, "coherent": 32, "coherent16": 16, "coherent64": 64, "ballot": 32}[trav]
     want = r_vis if width == 1 else np.repeat(T.group_visits(theta, eps, width), width)[: T.n]
     assert np.array_equal(u32(vis)[T.perm], want)
+
+
+# ---------------------------------------------------------------------------
+# slices of the sorted targets (orrery_bh_forces_range): the unit a caller
+# shards; aligned slices tiling [0, n) reproduce the full evaluation exactly
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("traversal", ["coherent64", "coherent", "coherent16", "independent", "together"])
+def test_target_slices(tt, traversal):
+    pos, mass, cap, T = case("ragged_5003_cap7")
+    p, m = dev(pos), dev(mass)
+    n = T.n
+    for fast in (False, True):
+        f_acc, f_inter, f_vis = tt.bh_forces(p, m, 0.5, EPS, cap, traversal, fast_term=fast)
+
+        def fresh():
+            return (torch.full((n, 3), float("nan"), device="cuda"),
+                    torch.full((n, 2), -1, dtype=torch.int32, device="cuda"),
+                    torch.full((n,), -1, dtype=torch.int32, device="cuda"))
+
+        for world in (1, 3, 4):
+            out = fresh()
+            for r in range(world):
+                tt.bh_forces(p, m, 0.5, EPS, cap, traversal, out=out, fast_term=fast,
+                             targets=tt.shard(n, r, world, 64))
+            assert torch.equal(out[0].view(torch.int32), f_acc.view(torch.int32))
+            assert torch.equal(out[1], f_inter) and torch.equal(out[2], f_vis)
+        # an empty slice writes nothing
+        out = fresh()
+        tt.bh_forces(p, m, 0.5, EPS, cap, traversal, out=out, fast_term=fast, targets=(100, 100))
+        assert bool(torch.isnan(out[0]).all()) and bool((out[1] == -1).all())
+        if traversal == "together":
+            continue  # its sums depend on the group, which an unaligned slice changes
+        # an unaligned slice: only its targets are written, with the full
+        # evaluation's sums and counts; its groups start at the slice, so a
+        # visit count is the union over other neighbours, never below the
+        # target's own walk
+        b, e = 77, 1234
+        out = fresh()
+        tt.bh_forces(p, m, 0.5, EPS, cap, traversal, out=out, fast_term=fast, targets=(b, e))
+        mine = torch.from_numpy(T.perm[b:e].astype(np.int64)).cuda()
+        rest = torch.ones(n, dtype=torch.bool, device="cuda")
+        rest[mine] = False
+        assert torch.equal(out[0][mine].view(torch.int32), f_acc[mine].view(torch.int32))
+        assert torch.equal(out[1][mine], f_inter[mine])
+        assert bool(torch.isnan(out[0][rest]).all()) and bool((out[1][rest] == -1).all())
+        assert bool((out[2][rest] == -1).all())
+        own = tt.bh_forces(p, m, 0.5, EPS, cap, "independent")[2]
+        assert bool((out[2][mine] >= own[mine]).all())
+    with pytest.raises(tt.OrreryError):
+        tt.bh_forces(p, m, 0.5, EPS, cap, traversal, targets=(10, 5))
+
+
+def test_target_slices_full_size(tt):
+    # two halves of the 1M workload on one GPU, each through the graph path
+    # twice: together the full evaluation, bit for bit
+    pos, mass = plummer(1048576, PAGES_SEED)
+    p, m = dev(pos), dev(mass)
+    n = pos.shape[0]
+    for fast in (False, True):
+        f = tt.bh_forces(p, m, 0.5, EPS, 32, "coherent64", fast_term=fast)
+        out = (torch.empty((n, 3), device="cuda"), torch.empty((n, 2), dtype=torch.int32, device="cuda"),
+               torch.empty((n,), dtype=torch.int32, device="cuda"))
+        for _ in range(2):
+            for r in range(2):
+                tt.bh_forces(p, m, 0.5, EPS, 32, "coherent64", out=out, fast_term=fast,
+                             targets=tt.shard(n, r, 2, 64))
+            assert torch.equal(out[0].view(torch.int32), f[0].view(torch.int32))
+            assert torch.equal(out[1], f[1]) and torch.equal(out[2], f[2])

@@ -8,7 +8,7 @@ this package is the thin Python binding over that library.
 
     from tree_traversal_gb300 import bh_forces
     acc, interactions, visits = bh_forces(pos, mass, theta=0.5, eps=0.05,
-                                          leaf_cap=32, traversal="coherent")
+                                          leaf_cap=32, traversal="coherent64")
 """
 from .bh import (  # noqa: F401
     bh_forces,
@@ -19,5 +19,6 @@ from .bh import (  # noqa: F401
     last_timings,
     max_nodes,
     release,
+    shard,
 )
 from ._lib import OrreryError, load  # noqa: F401

@@ -83,6 +83,8 @@ def load(path: str | None = None):
         i64, i32, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
         lib.orrery_bh_forces.argtypes = [P, P, i64, f32, f32, i32, i32, P, P, P, P]
         lib.orrery_bh_forces.restype = ctypes.c_int
+        lib.orrery_bh_forces_range.argtypes = [P, P, i64, f32, f32, i32, i32, i64, i64, P, P, P, P]
+        lib.orrery_bh_forces_range.restype = ctypes.c_int
         lib.orrery_bh_forces_host.argtypes = [P, P, i64, f32, f32, i32, i32, P, P, P, P]
         lib.orrery_bh_forces_host.restype = ctypes.c_int
         lib.orrery_bh_forces_noalloc.argtypes = [P, P, i64, f32, f32, i32, i32, P, P, P, P]

@@ -44,7 +44,7 @@ def _ptr(t):
 
 def bh_forces(pos: torch.Tensor, mass: torch.Tensor, theta: float = 0.5, eps: float = 0.05,
               leaf_cap: int = 32, traversal="coherent", counters: bool = True, out=None,
-              fast_term: bool = False):
+              fast_term: bool = False, targets=None):
     """Accelerations of n particles (caller order) on the current CUDA stream.
 
     pos [n, 3] float32, mass [n] float32, both CUDA and contiguous.
@@ -53,7 +53,9 @@ def bh_forces(pos: torch.Tensor, mass: torch.Tensor, theta: float = 0.5, eps: fl
     uint32 values stored in int32 tensors (they never exceed 2^31).
     ``out`` may pass preallocated (acc, interactions, visits) tensors.
     ``fast_term`` selects the approximate inverse square root (ORRERY_FAST_TERM):
-    faster, equal to the exact path to rounding rather than bit for bit."""
+    faster, equal to the exact path to rounding rather than bit for bit.
+    ``targets`` = (begin, end) walks only the sorted targets [begin, end)
+    (orrery_bh_forces_range): only their entries of the outputs are written."""
     n = int(pos.shape[0]) if pos.dim() == 2 else -1
     _check_device(pos, "pos", (n, 3))
     _check_device(mass, "mass", (n,))
@@ -71,14 +73,35 @@ def bh_forces(pos: torch.Tensor, mass: torch.Tensor, theta: float = 0.5, eps: fl
         _check_device(inter, "interactions", (n, 2), torch.int32)
     if visits is not None:
         _check_device(visits, "visits", (n,), torch.int32)
+    flags = _traversal(traversal) | (_lib.FAST_TERM if fast_term else 0)
     with torch.cuda.device(dev):
-        rc = _lib.load().orrery_bh_forces(
-            _ptr(pos), _ptr(mass), n, float(theta), float(eps), int(leaf_cap),
-            _traversal(traversal) | (_lib.FAST_TERM if fast_term else 0), _ptr(acc), _ptr(inter),
-            _ptr(visits), _stream_handle(dev))
+        if targets is None:
+            rc = _lib.load().orrery_bh_forces(
+                _ptr(pos), _ptr(mass), n, float(theta), float(eps), int(leaf_cap), flags,
+                _ptr(acc), _ptr(inter), _ptr(visits), _stream_handle(dev))
+            name = "orrery_bh_forces"
+        else:
+            begin, end = (int(v) for v in targets)
+            rc = _lib.load().orrery_bh_forces_range(
+                _ptr(pos), _ptr(mass), n, float(theta), float(eps), int(leaf_cap), flags,
+                begin, end, _ptr(acc), _ptr(inter), _ptr(visits), _stream_handle(dev))
+            name = "orrery_bh_forces_range"
     if rc != _lib.OK:
-        raise _lib.OrreryError(rc, "orrery_bh_forces")
+        raise _lib.OrreryError(rc, name)
     return acc, inter, visits
+
+
+def shard(n: int, rank: int, world: int, align: int = 64) -> tuple[int, int]:
+    """The sorted-target slice [begin, end) of rank ``rank`` of ``world`` when
+    one evaluation is split into equal slices whose edges are multiples of
+    ``align`` (the coherence width, so every rank reports the full
+    evaluation's visit counts); the slices tile [0, n)."""
+    if world < 1 or not 0 <= rank < world or n < 0 or align < 1:
+        raise ValueError("invalid shard arguments")
+    groups = -(-n // align)
+    lo = groups * rank // world
+    hi = groups * (rank + 1) // world
+    return min(n, lo * align), min(n, hi * align)
 
 
 def bh_forces_host(pos: np.ndarray, mass: np.ndarray, theta: float = 0.5, eps: float = 0.05,

@@ -45,14 +45,15 @@ enum Ev {
 struct GraphKey {
     const void *pos, *mass, *base;
     void *acc, *inter, *visits;
-    int64_t n;
+    int64_t n, t_begin, t_end;
     float theta, eps;
     int32_t cap, traversal;
     bool operator==(const GraphKey &o) const
     {
         return pos == o.pos && mass == o.mass && base == o.base && acc == o.acc &&
-               inter == o.inter && visits == o.visits && n == o.n && theta == o.theta &&
-               eps == o.eps && cap == o.cap && traversal == o.traversal;
+               inter == o.inter && visits == o.visits && n == o.n && t_begin == o.t_begin &&
+               t_end == o.t_end && theta == o.theta && eps == o.eps && cap == o.cap &&
+               traversal == o.traversal;
     }
 };
 
@@ -291,13 +292,14 @@ struct HostOut {
 // Enqueues phases a1..a8, for the host entry point the result copies, and
 // the read-back of the status word.
 void enqueue_forces(Workspace &w, const float *pos, const float *mass, int64_t n, float theta,
-                    float eps, int32_t cap, int32_t traversal, float *acc, uint32_t *inter,
-                    uint32_t *visits, cudaStream_t st, const HostOut *host)
+                    float eps, int32_t cap, int32_t traversal, int64_t t_begin, int64_t t_end,
+                    float *acc, uint32_t *inter, uint32_t *visits, cudaStream_t st,
+                    const HostOut *host)
 {
     uint64_t *keys_sorted = nullptr;
     uint32_t *perm = nullptr;
     run_tree(w, pos, mass, cap, st, &keys_sorted, &perm);
-    launch_walk(traversal, theta, eps, perm, w.b, acc, inter, visits, st);
+    launch_walk(traversal, theta, eps, perm, w.b, t_begin, t_end, acc, inter, visits, st);
     record_event(w.ev[EV_WALK], st);
     record_event(w.ev[EV_SCATTER], st);  // the scatter is fused into the walk
     if (host) {
@@ -329,7 +331,8 @@ int collect(Workspace &w, cudaStream_t st)
 // workspace's own stream, so it never touches the caller's stream.
 GraphEntry *graph_for(Workspace &w, const GraphKey &key, const float *pos, const float *mass,
                       int64_t n, float theta, float eps, int32_t cap, int32_t traversal,
-                      float *acc, uint32_t *inter, uint32_t *visits)
+                      int64_t t_begin, int64_t t_end, float *acc, uint32_t *inter,
+                      uint32_t *visits)
 {
     if (!graphs_enabled()) return nullptr;
     for (auto &g : w.graphs)
@@ -349,7 +352,7 @@ GraphEntry *graph_for(Workspace &w, const GraphKey &key, const float *pos, const
         cudaGetLastError();
         return nullptr;
     }
-    enqueue_forces(w, pos, mass, n, theta, eps, cap, traversal, acc, inter, visits,
+    enqueue_forces(w, pos, mass, n, theta, eps, cap, traversal, t_begin, t_end, acc, inter, visits,
                    w.capture_stream, nullptr);
     cudaGraph_t graph = nullptr;
     const cudaError_t ec = cudaStreamEndCapture(w.capture_stream, &graph);
@@ -378,20 +381,24 @@ GraphEntry *graph_for(Workspace &w, const GraphKey &key, const float *pos, const
 // arguments of an earlier one (device buffers only), else launches directly;
 // then blocks once and records the phase timings.
 int forces_device(Workspace &w, const float *pos, const float *mass, int64_t n, float theta,
-                  float eps, int32_t cap, int32_t traversal, float *acc, uint32_t *inter,
-                  uint32_t *visits, cudaStream_t st, const HostOut *host)
+                  float eps, int32_t cap, int32_t traversal, int64_t t_begin, int64_t t_end,
+                  float *acc, uint32_t *inter, uint32_t *visits, cudaStream_t st,
+                  const HostOut *host)
 {
     const uint64_t launches0 = g_launches.load();
     GraphEntry *g = nullptr;
     if (!host) {
-        const GraphKey key{pos, mass, w.base, acc, inter, visits, n, theta, eps, cap, traversal};
-        g = graph_for(w, key, pos, mass, n, theta, eps, cap, traversal, acc, inter, visits);
+        const GraphKey key{pos, mass, w.base, acc, inter, visits, n, t_begin, t_end,
+                           theta, eps, cap, traversal};
+        g = graph_for(w, key, pos, mass, n, theta, eps, cap, traversal, t_begin, t_end, acc, inter,
+                      visits);
     }
     if (g && cudaGraphLaunch(g->exec, st) == cudaSuccess) {
         g_launches += g->launches;
     } else {
         if (g) cudaGetLastError();
-        enqueue_forces(w, pos, mass, n, theta, eps, cap, traversal, acc, inter, visits, st, host);
+        enqueue_forces(w, pos, mass, n, theta, eps, cap, traversal, t_begin, t_end, acc, inter,
+                       visits, st, host);
     }
     const int rc = collect(w, st);
     if (rc != ORRERY_OK) return rc;
@@ -439,7 +446,25 @@ int orrery_bh_forces(const float *pos_d, const float *mass_d, int64_t n, float t
     Workspace *w = nullptr;
     rc = get_workspace(n, node_bound(n, leaf_cap), &w);
     if (rc != ORRERY_OK) return rc;
-    return forces_device(*w, pos_d, mass_d, n, theta, eps, leaf_cap, traversal, acc_d,
+    return forces_device(*w, pos_d, mass_d, n, theta, eps, leaf_cap, traversal, 0, n, acc_d,
+                         interactions_d, visits_d, (cudaStream_t)stream, nullptr);
+}
+
+int orrery_bh_forces_range(const float *pos_d, const float *mass_d, int64_t n, float theta,
+                           float eps, int32_t leaf_cap, int32_t traversal, int64_t begin,
+                           int64_t end, float *acc_d, uint32_t *interactions_d, uint32_t *visits_d,
+                           void *stream)
+{
+    int rc = check_args(n, theta, eps, leaf_cap, traversal);
+    if (rc != ORRERY_OK) return rc;
+    if (begin < 0 || end < begin || end > n) return ORRERY_EINVAL;
+    if (n == 0) return ORRERY_OK;
+    if (!pos_d || !mass_d || !acc_d) return ORRERY_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace *w = nullptr;
+    rc = get_workspace(n, node_bound(n, leaf_cap), &w);
+    if (rc != ORRERY_OK) return rc;
+    return forces_device(*w, pos_d, mass_d, n, theta, eps, leaf_cap, traversal, begin, end, acc_d,
                          interactions_d, visits_d, (cudaStream_t)stream, nullptr);
 }
 
@@ -483,7 +508,7 @@ int orrery_bh_forces_host(const float *pos, const float *mass, int64_t n, float 
     cudaMemcpyAsync(pos_d, pos, 12 * (size_t)n, cudaMemcpyHostToDevice, st);
     cudaMemcpyAsync(mass_d, mass, 4 * (size_t)n, cudaMemcpyHostToDevice, st);
     const HostOut host{acc, interactions, visits};
-    return forces_device(*w, pos_d, mass_d, n, theta, eps, leaf_cap, traversal, acc_d,
+    return forces_device(*w, pos_d, mass_d, n, theta, eps, leaf_cap, traversal, 0, n, acc_d,
                          interactions ? inter_d : nullptr, visits ? vis_d : nullptr, st, &host);
 }
 

@@ -80,9 +80,11 @@ void launch_gather(const float *pos, const float *mass, const uint32_t *perm, co
 void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b,
                   cudaStream_t st);
 void launch_moments(const Buffers &b, cudaStream_t st);
-// a7 with the a8 scatter fused: results land in the caller's order
+// a7 with the a8 scatter fused: results land in the caller's order. Walks
+// the sorted targets [t_begin, t_end) against the whole tree.
 void launch_walk(int traversal, float theta, float eps, const uint32_t *perm, const Buffers &b,
-                 float *acc, uint32_t *inter, uint32_t *visits, cudaStream_t st);
+                 int64_t t_begin, int64_t t_end, float *acc, uint32_t *inter, uint32_t *visits,
+                 cudaStream_t st);
 void launch_direct(const float *pos, const float *mass, int64_t n, float eps, float *acc,
                    int *status, cudaStream_t st);
 void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *partial,

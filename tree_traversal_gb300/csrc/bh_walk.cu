@@ -58,7 +58,8 @@ struct WalkArgs {
     const float4 *com;     // {CoM_x, CoM_y, CoM_z, M}
     const int4 *wnode;     // {escape, first, leaf count or 0, squared side bits}
     const uint32_t *perm;  // caller index of each sorted slot
-    int n;
+    int n;                 // particles (sources)
+    int t_begin, t_end;    // the sorted targets walked: [t_begin, t_end)
     float theta2;
     float eps2;
     DeviceParams *P;
@@ -196,8 +197,8 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
     const int lane = threadIdx.x & 31;
     const int glane = lane & (G - 1);
     const unsigned gmask = (G == 32) ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
-    const int tgt = blockIdx.x * kThreads + threadIdx.x;
-    const bool valid = tgt < a.n;
+    const int tgt = a.t_begin + blockIdx.x * kThreads + threadIdx.x;
+    const bool valid = tgt < a.t_end;
     const float4 xi = valid ? __ldg(a.ps + tgt) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     int next = valid ? 0 : num_nodes;
     float ax = 0.0f, ay = 0.0f, az = 0.0f;
@@ -336,9 +337,9 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
 {
     constexpr unsigned kFull = 0xffffffffu;
     const int lane = threadIdx.x & 31;
-    const int base = ((blockIdx.x * kThreads + threadIdx.x) >> 5) * 64;
+    const int base = a.t_begin + ((blockIdx.x * kThreads + threadIdx.x) >> 5) * 64;
     const int t0 = base + lane, t1 = base + 32 + lane;
-    const bool v0 = t0 < a.n, v1 = t1 < a.n;
+    const bool v0 = t0 < a.t_end, v1 = t1 < a.t_end;
     const float4 p0 = v0 ? __ldg(a.ps + t0) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     const float4 p1 = v1 ? __ldg(a.ps + t1) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     // negated positions: every separation is then one packed add
@@ -426,8 +427,8 @@ template <bool kCount, bool kSelfFree, bool kFast>
 __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, float4 *stage)
 {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kThreads + threadIdx.x;
-    const bool valid = t < a.n;
+    const int t = a.t_begin + blockIdx.x * kThreads + threadIdx.x;
+    const bool valid = t < a.t_end;
     const float4 xi = valid ? __ldg(a.ps + t) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     float ax = 0.0f, ay = 0.0f, az = 0.0f;
     uint32_t pc = 0, pp = 0;
@@ -497,8 +498,8 @@ __global__ void __launch_bounds__(kThreads) k_walk_together(WalkArgs a)
 template <bool kCount, bool kSelfFree, bool kFast>
 __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_nodes)
 {
-    const int t = blockIdx.x * kThreads + threadIdx.x;
-    if (t >= a.n) return;
+    const int t = a.t_begin + blockIdx.x * kThreads + threadIdx.x;
+    if (t >= a.t_end) return;
     const float4 xi = __ldg(a.ps + t);
     float ax = 0.0f, ay = 0.0f, az = 0.0f;
     uint32_t pc = 0, pp = 0;
@@ -558,7 +559,7 @@ void launch_kernels(int traversal, bool count, unsigned grid, const WalkArgs &a,
     case 1: coherent(std::integral_constant<int, 32>{}); break;
     case 2: coherent(std::integral_constant<int, 16>{}); break;
     case 3: {
-        const unsigned g = ceil_div(a.n, (int64_t)kThreads * 2);  // 64 targets per warp
+        const unsigned g = ceil_div(a.t_end - a.t_begin, (int64_t)kThreads * 2);  // 64 targets per warp
         if (count)
             k_walk_paired<true, kFast><<<g, kThreads, 0, st>>>(a);
         else
@@ -588,8 +589,10 @@ void launch_kernels(int traversal, bool count, unsigned grid, const WalkArgs &a,
 }  // namespace
 
 void launch_walk(int traversal_flags, float theta, float eps, const uint32_t *perm,
-                 const Buffers &b, float *acc, uint32_t *inter, uint32_t *visits, cudaStream_t st)
+                 const Buffers &b, int64_t t_begin, int64_t t_end, float *acc, uint32_t *inter,
+                 uint32_t *visits, cudaStream_t st)
 {
+    if (t_end <= t_begin) return;  // no targets: nothing to launch
     const int traversal = traversal_flags & kTraversalMask;
     const bool fast = (traversal_flags & kFastTermFlag) != 0;
     const bool count = inter != nullptr || visits != nullptr;
@@ -599,13 +602,15 @@ void launch_walk(int traversal_flags, float theta, float eps, const uint32_t *pe
     a.wnode = b.wnode;
     a.perm = perm;
     a.n = (int)b.n;
+    a.t_begin = (int)t_begin;
+    a.t_end = (int)t_end;
     a.theta2 = theta * theta;  // host binary32 products, round to nearest
     a.eps2 = eps * eps;
     a.P = b.params;
     a.acc = acc;
     a.inter = inter;
     a.visits = visits;
-    const unsigned grid = ceil_div(b.n, kThreads);
+    const unsigned grid = ceil_div(t_end - t_begin, kThreads);
     if (fast)
         launch_kernels<true>(traversal, count, grid, a, st);
     else
