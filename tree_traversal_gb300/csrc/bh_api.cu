@@ -152,8 +152,7 @@ size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
     b.nchild = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
     b.arrive = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
     b.sums = (float4 *)take(sizeof(float4) * (size_t)nodes);
-    b.com = (float4 *)take(sizeof(float4) * (size_t)nodes);
-    b.wnode = (int4 *)take(sizeof(int4) * (size_t)nodes);
+    b.wnode = (WalkNode *)take(sizeof(WalkNode) * (size_t)nodes);
     return off;
 }
 
@@ -540,8 +539,9 @@ int orrery_bh_tree(const float *pos_d, const float *mass_d, int64_t n, int32_t l
     const int64_t nc = nn < max_nodes ? nn : max_nodes;
     if (nodes_d && nc > 0)
         cudaMemcpyAsync(nodes_d, w->b.meta, 16 * (size_t)nc, cudaMemcpyDeviceToDevice, st);
-    if (com_d && nc > 0)
-        cudaMemcpyAsync(com_d, w->b.com, 16 * (size_t)nc, cudaMemcpyDeviceToDevice, st);
+    if (com_d && nc > 0)  // the {CoM, M} half of each 32-byte walk node
+        cudaMemcpy2DAsync(com_d, sizeof(float4), &w->b.wnode[0].c, sizeof(WalkNode),
+                          sizeof(float4), (size_t)nc, cudaMemcpyDeviceToDevice, st);
     if (cudaStreamSynchronize(st) != cudaSuccess || cudaGetLastError() != cudaSuccess)
         return ORRERY_ECUDA;
     return nn > max_nodes ? ORRERY_ERANGE : ORRERY_OK;

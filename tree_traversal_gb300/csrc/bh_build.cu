@@ -132,8 +132,8 @@ k_build_emit(const uint64_t *__restrict__ K, int64_t n, const int8_t *__restrict
 // A node whose mass is not finite or whose CoM lies at 2^126 or beyond is
 // reported as non-finite: with every coordinate below 2^125 (checked with the
 // bounding box), every separation the walks form is then a finite number.
-__device__ __forceinline__ void store_moments(int64_t k, float sx, float sy, float sz, float M,
-                                              float4 *sums, float4 *com, DeviceParams *P)
+__device__ __forceinline__ float4 store_moments(int64_t k, float sx, float sy, float sz, float M,
+                                                float4 *sums, DeviceParams *P)
 {
     __stcg(sums + k, make_float4(sx, sy, sz, M));
     float4 c = make_float4(0.0f, 0.0f, 0.0f, M);
@@ -145,17 +145,17 @@ __device__ __forceinline__ void store_moments(int64_t k, float sx, float sy, flo
     const float lim = 0x1p126f;
     if (!(fabsf(M) <= FLT_MAX && fabsf(c.x) < lim && fabsf(c.y) < lim && fabsf(c.z) < lim))
         atomicOr((int *)&P->status, kStatusNonFinite);
-    __stcg(com + k, c);
+    return c;
 }
 
 // Stores a node's moments and its walk record {escape, first, leaf count
 // (0 for an internal node), bits of (side 2^-level)^2}.
 __device__ __forceinline__ void store_node(int64_t k, const int4 &m, bool leaf, float sx, float sy,
-                                           float sz, float M, float4 *sums, float4 *com,
-                                           int4 *wnode, DeviceParams *P)
+                                           float sz, float M, float4 *sums,
+                                           WalkNode *wnode, DeviceParams *P)
 {
-    wnode[k] = make_int4(m.x, m.y, leaf ? m.z : 0, __float_as_int(P->s2[m.w]));
-    store_moments(k, sx, sy, sz, M, sums, com, P);
+    wnode[k].w = make_int4(m.x, m.y, leaf ? m.z : 0, __float_as_int(P->s2[m.w]));
+    wnode[k].c = store_moments(k, sx, sy, sz, M, sums, P);
 }
 
 // a6: one thread per leaf (the last node of each position's chain) sums its
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads)
 k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ ncount,
           const uint32_t *__restrict__ node_start, const int4 *__restrict__ meta,
           const int32_t *__restrict__ parent, const int32_t *__restrict__ nchild,
-          int32_t *__restrict__ arrive, float4 *sums, float4 *com, int4 *__restrict__ wnode,
+          int32_t *__restrict__ arrive, float4 *sums, WalkNode *__restrict__ wnode,
           DeviceParams *P)
 {
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -188,7 +188,7 @@ k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ 
         sy = __fmaf_rn(p.w, p.y, sy);
         sz = __fmaf_rn(p.w, p.z, sz);
     }
-    store_node(k, m, true, sx, sy, sz, M, sums, com, wnode, P);
+    store_node(k, m, true, sx, sy, sz, M, sums, wnode, P);
     int64_t node = parent[k];
     while (node >= 0) {
         __threadfence();
@@ -214,7 +214,7 @@ k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ 
             }
             c = nc;
         }
-        store_node(node, meta[node], false, sx, sy, sz, M, sums, com, wnode, P);
+        store_node(node, meta[node], false, sx, sy, sz, M, sums, wnode, P);
         node = parent[node];
     }
 }
@@ -241,7 +241,7 @@ void launch_moments(const Buffers &b, cudaStream_t st)
     cudaMemsetAsync(b.arrive, 0, sizeof(int32_t) * (size_t)b.max_nodes, st);
     k_moments<<<ceil_div(b.n, kThreads), kThreads, 0, st>>>(b.ps, b.n, b.ncount, b.node_start,
                                                            b.meta, b.parent, b.nchild, b.arrive,
-                                                           b.sums, b.com, b.wnode, b.params);
+                                                           b.sums, b.wnode, b.params);
     g_launches += 1;
 }
 

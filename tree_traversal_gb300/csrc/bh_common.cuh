@@ -35,6 +35,14 @@ struct DeviceParams {
 };
 
 // Device pointers carved out of one workspace allocation.
+// One node as the walks read it: 32 bytes, one sector, so a step's two
+// 16-byte loads touch one cache line. w = {escape, first, leaf count or 0,
+// bits of the node's squared side}; c = {CoM_x, CoM_y, CoM_z, M}.
+struct alignas(32) WalkNode {
+    int4 w;
+    float4 c;
+};
+
 struct Buffers {
     int64_t n;
     int64_t max_nodes;
@@ -63,9 +71,7 @@ struct Buffers {
     int32_t *arrive;          // [max_nodes]
     // a6
     float4 *sums;             // [max_nodes] {S_x, S_y, S_z, M}
-    float4 *com;              // [max_nodes] {CoM_x, CoM_y, CoM_z, M}
-    int4 *wnode;              // [max_nodes] walk record {escape, first, leaf count or 0,
-                              //  bits of the node's squared side}
+    WalkNode *wnode;          // [max_nodes] everything a walk step reads of a node
 };
 
 // Kernel-launch counter (every launch site increments it).

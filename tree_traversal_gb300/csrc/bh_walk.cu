@@ -55,8 +55,7 @@ constexpr int kWarpsPerBlock = kThreads / 32;
 
 struct WalkArgs {
     const float4 *ps;      // sorted particles {x, y, z, m}
-    const float4 *com;     // {CoM_x, CoM_y, CoM_z, M}
-    const int4 *wnode;     // {escape, first, leaf count or 0, squared side bits}
+    const WalkNode *wnode; // {escape, first, leaf count or 0, squared side bits}, {CoM, M}
     const uint32_t *perm;  // caller index of each sorted slot
     int n;                 // particles (sources)
     int t_begin, t_end;    // the sorted targets walked: [t_begin, t_end)
@@ -208,8 +207,8 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
     for (; steps <= num_nodes; ++steps) {
         const int k = kBallot ? kb : __reduce_min_sync(gmask, next);
         if (k >= num_nodes) break;
-        const float4 c = __ldg(a.com + k);
-        const int4 w = __ldg(a.wnode + k);
+        const int4 w = __ldg(&a.wnode[k].w);
+        const float4 c = __ldg(&a.wnode[k].c);
         bool open = false, descend = false;
         if (next == k) {
             const float dx = __fsub_rn(c.x, xi.x);
@@ -353,8 +352,8 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
     for (; steps <= num_nodes; ++steps) {
         const int k = __reduce_min_sync(kFull, min(next0, next1));
         if (k >= num_nodes) break;
-        const float4 c = __ldg(a.com + k);
-        const int4 w = __ldg(a.wnode + k);
+        const int4 w = __ldg(&a.wnode[k].w);
+        const float4 c = __ldg(&a.wnode[k].c);
         const bool act0 = next0 == k, act1 = next1 == k;
         const Sep2 s = separation2(c.x, c.y, c.z, nx, ny, nz);
         const float2 lim = __fmul2_rn(theta2, s.d2);
@@ -434,8 +433,8 @@ __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, 
     uint32_t pc = 0, pp = 0;
     int k = 0, steps = 0;
     for (; k < num_nodes && steps <= num_nodes; ++steps) {
-        const float4 c = __ldg(a.com + k);
-        const int4 w = __ldg(a.wnode + k);
+        const int4 w = __ldg(&a.wnode[k].w);
+        const float4 c = __ldg(&a.wnode[k].c);
         const float dx = __fsub_rn(c.x, xi.x);
         const float dy = __fsub_rn(c.y, xi.y);
         const float dz = __fsub_rn(c.z, xi.z);
@@ -505,8 +504,8 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
     uint32_t pc = 0, pp = 0;
     int k = 0, steps = 0;
     for (; steps <= num_nodes && k < num_nodes; ++steps) {
-        const float4 c = __ldg(a.com + k);
-        const int4 w = __ldg(a.wnode + k);
+        const int4 w = __ldg(&a.wnode[k].w);
+        const float4 c = __ldg(&a.wnode[k].c);
         const float dx = __fsub_rn(c.x, xi.x);
         const float dy = __fsub_rn(c.y, xi.y);
         const float dz = __fsub_rn(c.z, xi.z);
@@ -598,7 +597,6 @@ void launch_walk(int traversal_flags, float theta, float eps, const uint32_t *pe
     const bool count = inter != nullptr || visits != nullptr;
     WalkArgs a;
     a.ps = b.ps;
-    a.com = b.com;
     a.wnode = b.wnode;
     a.perm = perm;
     a.n = (int)b.n;
