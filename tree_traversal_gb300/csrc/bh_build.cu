@@ -148,13 +148,15 @@ __device__ __forceinline__ float4 store_moments(int64_t k, float sx, float sy, f
     return c;
 }
 
-// Stores a node's moments and its walk record {escape, first, leaf count
-// (0 for an internal node), bits of (side 2^-level)^2}.
+// Stores a node's moments and its walk record {escape, the node a target
+// that does not accept it goes to next (escape for a leaf, which it opens;
+// k + 1 for an internal node, which it enters), leaf count (0 for an internal
+// node), bits of (side 2^-level)^2}.
 __device__ __forceinline__ void store_node(int64_t k, const int4 &m, bool leaf, float sx, float sy,
                                            float sz, float M, float4 *sums,
                                            WalkNode *wnode, DeviceParams *P)
 {
-    wnode[k].w = make_int4(m.x, m.y, leaf ? m.z : 0, __float_as_int(P->s2[m.w]));
+    wnode[k].w = make_int4(m.x, leaf ? m.x : (int)k + 1, leaf ? m.z : 0, __float_as_int(P->s2[m.w]));
     wnode[k].c = store_moments(k, sx, sy, sz, M, sums, P);
 }
 

@@ -36,8 +36,10 @@ struct DeviceParams {
 
 // Device pointers carved out of one workspace allocation.
 // One node as the walks read it: 32 bytes, one sector, so a step's two
-// 16-byte loads touch one cache line. w = {escape, first, leaf count or 0,
-// bits of the node's squared side}; c = {CoM_x, CoM_y, CoM_z, M}.
+// 16-byte loads touch one cache line. w = {escape, next node when not
+// accepted (escape for a leaf, k + 1 otherwise), leaf count or 0, bits of the
+// node's squared side}; c = {CoM_x, CoM_y, CoM_z, M}. A leaf's first particle
+// is read from the node table (meta) when the leaf is opened.
 struct alignas(32) WalkNode {
     int4 w;
     float4 c;

@@ -55,7 +55,8 @@ constexpr int kWarpsPerBlock = kThreads / 32;
 
 struct WalkArgs {
     const float4 *ps;      // sorted particles {x, y, z, m}
-    const WalkNode *wnode; // {escape, first, leaf count or 0, squared side bits}, {CoM, M}
+    const WalkNode *wnode; // {escape, next if not accepted, leaf count or 0, side^2 bits}, {CoM, M}
+    const int4 *meta;      // node table {escape, first, count, level}: a leaf's first particle
     const uint32_t *perm;  // caller index of each sorted slot
     int n;                 // particles (sources)
     int t_begin, t_end;    // the sorted targets walked: [t_begin, t_end)
@@ -221,13 +222,13 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
                 next = w.x;
             } else {
                 open = w.z != 0;
-                next = open ? w.x : k + 1;
+                next = w.y;
                 descend = !open;
             }
         }
         if (kBallot) kb = __any_sync(gmask, descend) ? k + 1 : w.x;
         if (__any_sync(gmask, open)) {
-            const int first = w.y, count = w.z;
+            const int first = __ldg(&a.meta[k].y), count = w.z;
             if (first < 0 || first > a.n - count) {  // group-uniform consistency check
                 if (glane == 0) atomicOr(&a.P->status, kStatusInternal);
                 break;
@@ -368,10 +369,10 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
         }
         const bool leaf = w.z != 0;
         const bool open0 = act0 && !acc0 && leaf, open1 = act1 && !acc1 && leaf;
-        if (act0) next0 = (acc0 || leaf) ? w.x : k + 1;
-        if (act1) next1 = (acc1 || leaf) ? w.x : k + 1;
+        if (act0) next0 = acc0 ? w.x : w.y;
+        if (act1) next1 = acc1 ? w.x : w.y;
         if (__any_sync(kFull, open0 || open1)) {
-            const int first = w.y, count = w.z;
+            const int first = __ldg(&a.meta[k].y), count = w.z;
             if (first < 0 || first > a.n - count) {  // warp-uniform consistency check
                 if (lane == 0) atomicOr(&a.P->status, kStatusInternal);
                 break;
@@ -447,7 +448,7 @@ __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, 
             }
             k = w.x;
         } else if (w.z != 0) {
-            const int first = w.y, count = w.z;
+            const int first = __ldg(&a.meta[k].y), count = w.z;
             if (first < 0 || first > a.n - count) {  // warp-uniform consistency check
                 if (lane == 0) atomicOr(&a.P->status, kStatusInternal);
                 break;
@@ -515,7 +516,7 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
             if (kCount) ++pc;
             k = w.x;
         } else if (w.z != 0) {
-            const int first = w.y, count = w.z;
+            const int first = __ldg(&a.meta[k].y), count = w.z;
             if (first < 0 || first > a.n - count) {
                 atomicOr(&a.P->status, kStatusInternal);
                 break;
@@ -598,6 +599,7 @@ void launch_walk(int traversal_flags, float theta, float eps, const uint32_t *pe
     WalkArgs a;
     a.ps = b.ps;
     a.wnode = b.wnode;
+    a.meta = b.meta;
     a.perm = perm;
     a.n = (int)b.n;
     a.t_begin = (int)t_begin;
