@@ -88,7 +88,7 @@ typedef enum {
 
 /* Flag ORed into the traversal argument: the force term's inverse square
  * root uses the hardware approximation (rsqrt.approx) instead of the fixed
- * Newton sequence. The width-64 walk is then ~15 % faster; acceptance
+ * Newton sequence. The width-64 walk is then ~20 % faster; acceptance
  * decisions, counts and visits are unchanged, and accelerations agree with
  * the exact path to rounding instead of bit for bit: at most 4.4e-6 relative
  * on the Plummer and two-sphere workloads (softening 0.05, 1M-2M particles),
