@@ -22,6 +22,8 @@
 // escape(node) = scan value at the first position past the node's range.
 #include <cfloat>
 
+#include <cuda/atomic>
+
 #include "bh_common.cuh"
 
 namespace obh {
@@ -193,10 +195,11 @@ k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ 
     store_node(k, m, true, sx, sy, sz, M, sums, wnode, P);
     int64_t node = parent[k];
     while (node >= 0) {
-        __threadfence();
-        const int prev = atomicAdd(arrive + node, 1);
+        // release: this child's sums before the count; acquire: the last
+        // child to arrive sees every sibling's sums
+        cuda::atomic_ref<int32_t, cuda::thread_scope_device> count(arrive[node]);
+        const int prev = count.fetch_add(1, cuda::std::memory_order_acq_rel);
         if (prev != nchild[node] - 1) return;
-        __threadfence();
         const int esc = meta[node].x;
         M = sx = sy = sz = 0.0f;
         if (esc > total) {

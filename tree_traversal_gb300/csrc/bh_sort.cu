@@ -212,6 +212,136 @@ k_radix_scatter(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ v
     }
 }
 
+// Up to 4096 keys: the whole sort in one block, all seven passes in
+// shared memory. Each pass ranks the keys exactly as the scatter above (per-
+// warp digit counts with match-any votes, spans and rounds walked in key
+// order, so equal digits keep their order), writes every key to its rank in
+// shared memory and reads its new keys back. One launch instead of 21: at
+// these sizes the sort is bound by launch latency, not by work.
+constexpr int kSmallThreads = 512;
+constexpr int kSmallWarps = kSmallThreads / 32;
+constexpr int kSmallItems = 8;                           // rounds per lane at most
+// 4096 keys at most: the cost grows with the rounds per lane (about 6 us per
+// round over the seven passes, scattering keys into shared memory; measured
+// 31 / 68 us at 1024 / 4096 keys against 76 / 101 us for the multi-block
+// passes), so beyond 4096 keys it would no longer win.
+constexpr int kSmallN = kSmallThreads * kSmallItems;     // 4096
+
+struct SmallSortSmem {
+    uint64_t key[kSmallN];
+    uint32_t val[kSmallN];
+    uint32_t cnt[kSmallWarps][kBins];  // per-warp digit counts, then offsets
+    uint32_t loc[kBins];               // start of each digit's run
+};
+
+// Exclusive scan of one value per thread over a 512-thread block.
+__device__ __forceinline__ uint32_t block_scan_512(uint32_t v, uint32_t &total)
+{
+    __shared__ uint32_t sums[kSmallWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) sums[warp] = x;
+    __syncthreads();
+    uint32_t before = 0;
+    total = 0;
+    for (int w = 0; w < kSmallWarps; ++w) {
+        if (w < warp) before += sums[w];
+        total += sums[w];
+    }
+    __syncthreads();
+    return before + x - v;
+}
+
+__global__ void __launch_bounds__(kSmallThreads)
+k_radix_sort_small(const uint64_t *__restrict__ kin, uint64_t *__restrict__ kout,
+                   uint32_t *__restrict__ vout, int n, int *status)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SmallSortSmem &S = *reinterpret_cast<SmallSortSmem *>(smem_raw);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    // each warp takes a contiguous span of rounds * 32 keys, just enough to
+    // cover n; rounds walk the span in key order (round-major, then lane)
+    const int rounds = (n + kSmallThreads - 1) / kSmallThreads;
+    const int span = warp * 32 * rounds;
+    uint64_t key[kSmallItems];
+    uint32_t val[kSmallItems];
+#pragma unroll
+    for (int r = 0; r < kSmallItems; ++r) {
+        const int e = span + r * 32 + lane;
+        key[r] = (r < rounds && e < n) ? kin[e] : 0ull;
+        val[r] = (uint32_t)e;
+    }
+    for (int pass = 0; pass < kPasses; ++pass) {
+        const int shift = kBits * pass;
+        for (int i = threadIdx.x; i < kSmallWarps * kBins; i += kSmallThreads) (&S.cnt[0][0])[i] = 0;
+        __syncthreads();
+        uint32_t dig[kSmallItems];
+#pragma unroll
+        for (int r = 0; r < kSmallItems; ++r) {  // per-warp digit counts
+            const int e = span + r * 32 + lane;
+            dig[r] = (r < rounds && e < n) ? digit_of(key[r], shift) : (uint32_t)kBins;
+            if (r >= rounds) continue;  // warp-uniform
+            const unsigned peers = __match_any_sync(0xffffffffu, dig[r]);
+            if (lane == __ffs(peers) - 1 && dig[r] < (uint32_t)kBins) S.cnt[warp][dig[r]] += __popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+        {  // thread d owns digit d: offsets of each warp's first key in the run
+            const int d = threadIdx.x;
+            uint32_t run = 0;
+            for (int w = 0; w < kSmallWarps; ++w) {
+                const uint32_t x = S.cnt[w][d];
+                S.cnt[w][d] = run;
+                run += x;
+            }
+            uint32_t all;
+            S.loc[d] = block_scan_512(run, all);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < kSmallItems; ++r) {  // every key to its stable rank
+            if (r >= rounds) break;  // warp-uniform
+            const unsigned peers = __match_any_sync(0xffffffffu, dig[r]);
+            if (dig[r] < (uint32_t)kBins) {
+                const uint32_t p = S.loc[dig[r]] + S.cnt[warp][dig[r]] + __popc(peers & lt);
+                if (p < (uint32_t)n) {
+                    S.key[p] = key[r];
+                    S.val[p] = val[r];
+                } else {
+                    atomicOr(status, kStatusInternal);
+                }
+            }
+            __syncwarp();
+            if (lane == __ffs(peers) - 1 && dig[r] < (uint32_t)kBins) S.cnt[warp][dig[r]] += __popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < kSmallItems; ++r) {  // read back in rank order
+            const int e = span + r * 32 + lane;
+            if (r < rounds && e < n) {
+                key[r] = S.key[e];
+                val[r] = S.val[e];
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int r = 0; r < kSmallItems; ++r) {
+        const int e = span + r * 32 + lane;
+        if (r < rounds && e < n) {
+            kout[e] = key[r];
+            vout[e] = val[r];
+        }
+    }
+}
+
 }  // namespace
 
 // Sorts b.keys_a (filled by the key phase) with the original indices as
@@ -224,6 +354,8 @@ void prepare_sort()
     if (dev < 0 || dev >= 64 || !configured[dev].load()) {
         cudaFuncSetAttribute(k_radix_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(ScatterSmem));
+        cudaFuncSetAttribute(k_radix_sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(SmallSortSmem));
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
 }
@@ -233,6 +365,14 @@ void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint
     const int nb = b.radix_blocks;
     const size_t smem = sizeof(ScatterSmem);
     prepare_sort();
+    if (b.n <= kSmallN) {  // one block, one launch; the result lands where the passes' would
+        k_radix_sort_small<<<1, kSmallThreads, sizeof(SmallSortSmem), st>>>(
+            b.keys_a, b.keys_b, b.idx_b, (int)b.n, &b.params->status);
+        g_launches += 1;
+        *keys_sorted = b.keys_b;
+        *perm = b.idx_b;
+        return;
+    }
     uint64_t *kin = b.keys_a, *kout = b.keys_b;
     uint32_t *vin = b.idx_a, *vout = b.idx_b;
     for (int p = 0; p < kPasses; ++p) {
