@@ -92,9 +92,11 @@ typedef enum {
  * decisions, counts and visits are unchanged, and accelerations agree with
  * the exact path to rounding instead of bit for bit: at most 4.4e-6 relative
  * on the Plummer and two-sphere workloads (softening 0.05, 1M-2M particles),
- * bounded by 1e-5 in the tests at softening 0.05 and above. Without softening
- * the per-term error can be multiplied by cancellation between close pairs
- * (1.6e-5 seen at eps = 1e-20), so the exact term is the one to use there.
+ * bounded by 1e-5 in the tests at softening 0.05 and above. In general the
+ * deviation of a target is a few 1e-7 of the summed magnitude of its terms,
+ * so a target whose terms nearly cancel shows a larger relative deviation
+ * (1.6e-5 seen without softening, 2.6e-5 at the centre of a uniform cube
+ * with theta 1.2): where that matters the exact term is the one to use.
  * Without the flag results are reproducible bit for bit on any IEEE-754 CPU. */
 #define ORRERY_FAST_TERM 0x100
 

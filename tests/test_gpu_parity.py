@@ -611,3 +611,48 @@ def test_target_slices_full_size(tt):
                              targets=tt.shard(n, r, 2, 64))
             assert torch.equal(out[0].view(torch.int32), f[0].view(torch.int32))
             assert torch.equal(out[1], f[1]) and torch.equal(out[2], f[2])
+
+
+def magnitude_sums(pos, mass, eps, targets):
+    """Sum over j != i of |m_j (x_j - x_i)| / (r^2 + eps^2)^1.5, in fp64: the
+    scale an error of the terms' inverse root is measured against."""
+    x = pos.astype(np.float64)
+    out = np.empty(len(targets))
+    for k, i in enumerate(targets):
+        d = x - x[i]
+        r2 = (d * d).sum(1)
+        w = mass.astype(np.float64) * np.sqrt(r2) / (r2 + eps * eps) ** 1.5
+        w[i] = 0.0
+        out[k] = w.sum()
+    return out
+
+
+@pytest.mark.parametrize("seed", range(24, 36))
+def test_random_configurations_fast_term_and_slices(tt, seed):
+    # the same seeded sweep through the fast term and through two aligned
+    # slices. Fast term: counts bit-exact; each target's deviation from the
+    # oracle within 1e-5 of the summed magnitude of its terms (the relative
+    # error of a target whose terms nearly cancel -- a uniform cube at a wide
+    # opening angle -- can exceed 1e-5; on the Plummer workloads the
+    # relative bound itself holds, see the tests above). Slices: bit-exact.
+    pos, mass, cap, theta, eps, trav = _random_config(seed)
+    eps = max(eps, 0.05)
+    T = oracle.Tree(pos, mass, cap)
+    r_acc, r_pc, r_pp, r_vis = T.walk(theta, eps, threads=oracle.default_threads())
+    p, m = dev(pos), dev(mass)
+    acc, inter, vis = tt.bh_forces(p, m, theta, eps, cap, trav, fast_term=True)
+    gi = u32(inter)[T.perm]
+    assert np.array_equal(gi[:, 0], r_pc) and np.array_equal(gi[:, 1], r_pp)
+    g = acc.cpu().numpy()[T.perm].astype(np.float64)
+    dev_norm = np.linalg.norm(g - r_acc.astype(np.float64), axis=1)
+    sample = np.random.default_rng(seed).choice(T.n, min(T.n, 256), replace=False)
+    scale = magnitude_sums(pos, mass, eps, T.perm[sample])
+    assert bool(np.all(dev_norm[sample] <= REL_TOL * scale))
+    exact = tt.bh_forces(p, m, theta, eps, cap, trav)
+    n = T.n
+    out = (torch.empty((n, 3), device="cuda"), torch.empty((n, 2), dtype=torch.int32, device="cuda"),
+           torch.empty((n,), dtype=torch.int32, device="cuda"))
+    for r in range(2):
+        tt.bh_forces(p, m, theta, eps, cap, trav, out=out, targets=tt.shard(n, r, 2, 64))
+    assert torch.equal(out[0].view(torch.int32), exact[0].view(torch.int32))
+    assert torch.equal(out[1], exact[1]) and torch.equal(out[2], exact[2])
