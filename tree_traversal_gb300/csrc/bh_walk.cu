@@ -10,7 +10,8 @@
 // to (the escape index) and contributes nothing until the group reaches it.
 // The group's visited sequence is therefore the union of its lanes' walks and
 // every target is summed over exactly its own nodes, in the same order, so
-// the two kernels below produce bit-identical sums and counters.
+// the independent and the coherent kernels below produce bit-identical sums
+// and counters.
 //
 // Per target i at node k of level L (a visit is one acceptance test):
 //   accept iff (side 2^-L)^2 < theta^2 |CoM_k - x_i|^2  -> cell term, escape
@@ -22,15 +23,17 @@
 // decisions and sums do not depend on contraction choices, and a CPU
 // restatement of the same steps reproduces them bit for bit.
 //
-// GB300 shape of the coherent kernel: the node k is group-uniform, so its two
-// 16-byte records are read once per group step and broadcast. The walk record
-// {escape, first, leaf count (0 = internal), squared side bits} carries
-// everything a step decides on, so a step needs no table lookup and no leaf
-// test beyond one compare. An opened leaf's particles are staged into shared
-// memory once (one coalesced 16-byte load per lane) and read back as
-// broadcasts by every lane that opened it. The loop is warp-uniform and
-// bounded: k strictly increases, so a walk takes at most num_nodes steps; the
-// loop stops there and raises a status bit rather than spin.
+// GB300 shape of the coherent kernels: the node k is group-uniform, so its
+// 32-byte record (one sector) is read once per group step and broadcast. The
+// record {escape, next node when not accepted, leaf count (0 = internal),
+// squared side bits; CoM, M} carries everything a step decides on, so a step
+// needs no table lookup and no select on the leaf flag. An opened leaf's
+// particles are staged into shared memory once (one coalesced 16-byte load
+// per lane) and read back as broadcasts by every lane that opened it. The
+// loop is warp-uniform and bounded: k strictly increases, so a walk takes at
+// most num_nodes steps; the loop stops there and raises a status bit rather
+// than spin. The default width-64 kernel (k_walk_paired, below) holds two
+// targets per lane and does their arithmetic in packed float2 instructions.
 //
 // The self term. When the target's own leaf is opened the oracle skips j = i.
 // Summing it instead changes nothing, bit for bit, whenever its force factor
