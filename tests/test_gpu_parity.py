@@ -656,3 +656,34 @@ def test_random_configurations_fast_term_and_slices(tt, seed):
         tt.bh_forces(p, m, theta, eps, cap, trav, out=out, targets=tt.shard(n, r, 2, 64))
     assert torch.equal(out[0].view(torch.int32), exact[0].view(torch.int32))
     assert torch.equal(out[1], exact[1]) and torch.equal(out[2], exact[2])
+
+
+def test_concurrent_callers_on_one_device(tt):
+    # calls from several host threads, each on its own stream, share the
+    # device's workspace under its lock: every result equals the lone call's
+    import threading
+
+    pos, mass, cap, T = case("ragged_5003_cap7")
+    p, m = dev(pos), dev(mass)
+    ref = tt.bh_forces(p, m, 0.5, EPS, cap, "coherent64")
+    errors, results = [], {}
+
+    def worker(i):
+        try:
+            with torch.cuda.stream(torch.cuda.Stream()):
+                for _ in range(5):
+                    got = tt.bh_forces(p, m, 0.5, EPS, cap, ("coherent64", "coherent", "independent")[i % 3])
+                torch.cuda.current_stream().synchronize()
+            results[i] = got
+        except Exception as e:  # reported below, in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(6)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i, got in results.items():
+        assert torch.equal(got[0].view(torch.int32), ref[0].view(torch.int32))
+        assert torch.equal(got[1], ref[1])

@@ -99,7 +99,10 @@ bool graphs_enabled()
     return on;
 }
 
-std::mutex g_mu;
+// Calls on one device are serialised (they share its workspace and graphs);
+// calls on different devices run concurrently.
+std::mutex g_dev_mu[kMaxDevices];
+std::mutex g_last_mu;  // guards g_last / g_have_last
 Workspace *g_ws[kMaxDevices] = {};
 orrery_bh_timings g_last{};
 bool g_have_last = false;
@@ -171,6 +174,17 @@ void free_workspace(Workspace *w)
         if (w->ev[e]) cudaEventDestroy(w->ev[e]);
     if (prev >= 0) cudaSetDevice(prev);
     delete w;
+}
+
+// The calling thread's current device, or -1.
+int current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return -1;
+    }
+    return dev;
 }
 
 // The calling thread's current device's workspace, grown to (n, nodes).
@@ -421,6 +435,7 @@ int forces_device(Workspace &w, const float *pos, const float *mass, int64_t n, 
     t.n = n;
     t.num_nodes = w.host_params->num_nodes;
     t.launches = g_launches.load() - launches0;
+    std::lock_guard<std::mutex> last(g_last_mu);
     g_last = t;
     g_have_last = true;
     return ORRERY_OK;
@@ -441,7 +456,9 @@ int orrery_bh_forces(const float *pos_d, const float *mass_d, int64_t n, float t
     if (rc != ORRERY_OK) return rc;
     if (n == 0) return ORRERY_OK;
     if (!pos_d || !mass_d || !acc_d) return ORRERY_EINVAL;
-    std::lock_guard<std::mutex> lock(g_mu);
+    const int dev = current_device();
+    if (dev < 0) return ORRERY_ECUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu[dev]);
     Workspace *w = nullptr;
     rc = get_workspace(n, node_bound(n, leaf_cap), &w);
     if (rc != ORRERY_OK) return rc;
@@ -459,7 +476,9 @@ int orrery_bh_forces_range(const float *pos_d, const float *mass_d, int64_t n, f
     if (begin < 0 || end < begin || end > n) return ORRERY_EINVAL;
     if (n == 0) return ORRERY_OK;
     if (!pos_d || !mass_d || !acc_d) return ORRERY_EINVAL;
-    std::lock_guard<std::mutex> lock(g_mu);
+    const int dev = current_device();
+    if (dev < 0) return ORRERY_ECUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu[dev]);
     Workspace *w = nullptr;
     rc = get_workspace(n, node_bound(n, leaf_cap), &w);
     if (rc != ORRERY_OK) return rc;
@@ -475,7 +494,9 @@ int orrery_bh_forces_host(const float *pos, const float *mass, int64_t n, float 
     if (rc != ORRERY_OK) return rc;
     if (n == 0) return ORRERY_OK;
     if (!pos || !mass || !acc) return ORRERY_EINVAL;
-    std::lock_guard<std::mutex> lock(g_mu);
+    const int dev = current_device();
+    if (dev < 0) return ORRERY_ECUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu[dev]);
     Workspace *w = nullptr;
     rc = get_workspace(n, node_bound(n, leaf_cap), &w);
     if (rc != ORRERY_OK) return rc;
@@ -521,7 +542,9 @@ int orrery_bh_tree(const float *pos_d, const float *mass_d, int64_t n, int32_t l
     *num_nodes = 0;
     if (n == 0) return ORRERY_OK;
     if (!pos_d || !mass_d) return ORRERY_EINVAL;
-    std::lock_guard<std::mutex> lock(g_mu);
+    const int dev = current_device();
+    if (dev < 0) return ORRERY_ECUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu[dev]);
     Workspace *w = nullptr;
     rc = get_workspace(n, node_bound(n, leaf_cap), &w);
     if (rc != ORRERY_OK) return rc;
@@ -553,7 +576,9 @@ int orrery_direct_forces(const float *pos_d, const float *mass_d, int64_t n, flo
     if (n < 0 || n > kMaxN || !(eps >= 0.0f)) return ORRERY_EINVAL;
     if (n == 0) return ORRERY_OK;
     if (!pos_d || !mass_d || !acc_d) return ORRERY_EINVAL;
-    std::lock_guard<std::mutex> lock(g_mu);
+    const int dev = current_device();
+    if (dev < 0) return ORRERY_ECUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu[dev]);
     Workspace *w = nullptr;
     int rc = get_workspace(1, node_bound(1, 1), &w);  // only the status word is used
     if (rc != ORRERY_OK) return rc;
@@ -575,7 +600,7 @@ int64_t orrery_bh_max_nodes(int64_t n, int32_t leaf_cap)
 int orrery_bh_last_timings(orrery_bh_timings *out)
 {
     if (!out) return ORRERY_EINVAL;
-    std::lock_guard<std::mutex> lock(g_mu);
+    std::lock_guard<std::mutex> lock(g_last_mu);
     if (!g_have_last) return ORRERY_EINVAL;
     *out = g_last;
     return ORRERY_OK;
@@ -601,11 +626,12 @@ const char *orrery_bh_strerror(int status)
 
 void orrery_bh_release(void)
 {
-    std::lock_guard<std::mutex> lock(g_mu);
     for (int d = 0; d < kMaxDevices; ++d) {
+        std::lock_guard<std::mutex> lock(g_dev_mu[d]);
         free_workspace(g_ws[d]);
         g_ws[d] = nullptr;
     }
+    std::lock_guard<std::mutex> last(g_last_mu);
     g_have_last = false;
 }
 
