@@ -294,12 +294,21 @@ def cpu_baseline(pos, mass, params, seconds: float) -> dict:
     inter_sample = float(pc.sum() + pp.sum())
     t_full = t_build + t_walk * n / len(tgt)
     inter_full = inter_sample * n / len(tgt)
+    # one thread, on every 64th target of that sample (the pages' protocol
+    # times the CPU both ways)
+    t0 = time.perf_counter()
+    sub = tgt[:: 64] if len(tgt) >= 64 else tgt
+    _, pc1, pp1, _ = T.walk(params["theta"], params["eps"], sub, threads=1)
+    t_walk1 = time.perf_counter() - t0
+    walk1_per_s = float(pc1.sum() + pp1.sum()) / t_walk1
     import platform
     return {"value": inter_full / t_full, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": "full tree build (%.2f s, 1 thread) + walks of %d of %d targets in whole "
                       "32-target groups (%.2f s, %d threads), scaled to all targets"
                       % (t_build, len(tgt), n, t_walk, threads),
-            "ms_per_evaluation_est": 1000.0 * t_full, "cpu": platform.machine()}
+            "ms_per_evaluation_est": 1000.0 * t_full, "cpu": platform.machine(),
+            "walk_interactions_per_s_1_thread": walk1_per_s,
+            "walk_interactions_per_s_all_threads": inter_sample / t_walk}
 
 
 def run_reference(args, rank: int, world: int) -> None:
@@ -503,7 +512,8 @@ def main():
                      "frac_incl_acceptance": (flops_inter + FLOPS_PER_VISIT * vis_ind * n)
                      / (walk_ms / 1000.0) / 1e12 / peak_tflops},
         "cpu_baseline": None if cb is None else
-        {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "walk_interactions_per_s_1_thread",
+                             "walk_interactions_per_s_all_threads")},
         "e2e": {"value": interactions / (statistics.median(e2e_ms) / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": 16 * n, "d2h_bytes_per_step": 24 * n,
                 "ms_median": statistics.median(e2e_ms), "h2d_ms": e2e_host["h2d_ms"],
@@ -512,6 +522,8 @@ def main():
                                            "build_ms", "moments_ms", "walk_ms", "scatter_ms",
                                            "total_ms")},
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms),
+                    "iqr": (statistics.quantiles(step_ms, n=4)[2] - statistics.quantiles(step_ms, n=4)[0])
+                    if len(step_ms) >= 2 else 0.0,
                     "wall_s_incl_flush": wall},
         "tree": {"num_nodes": phases[-1]["num_nodes"], "depth": phases[-1]["depth"]},
         "per_particle": {"interactions": interactions / n, "cells": pc_mean, "particles": pp_mean,
