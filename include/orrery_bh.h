@@ -25,18 +25,27 @@
  *              octant order; nodes in depth-first preorder
  *   moments:   leaf M = sum m, S = sum fma(m, x, S) in sorted order; internal
  *              nodes sum their children in order; CoM = S / M (0 if M <= 0)
- *   criterion: accept iff (side 2^-L)^2 < (theta^2) * |CoM - x_i|^2
- *   term:      r2 = |x_j - x_i|^2 + eps^2; y = the binary32 value nearest
- *              1/sqrt(r2); f = (m_j y)(y y); a_i += f (x_j - x_i), fused
- *              multiply-add, in walk order
- * Both traversals give bit-identical accelerations and counters.
+ *   criterion: accept iff (side 2^-L)^2 < (theta^2) * d2, d2 = |CoM - x_i|^2
+ *              formed as fma(dz, dz, fma(dy, dy, dx * dx))
+ *   term:      r2 = d2 + eps^2 (d2 of the source, cell CoM or particle);
+ *              y = 1/sqrt(r2) by a fixed recipe: the bit-level seed
+ *              0x5f375a86 - bits(r2)/2 (C. Lomont, 2003) and three
+ *              Newton-Raphson steps y (3/2 - (r2/2) y^2), within 2 ulp;
+ *              f = (m y)(y y); a_i += f (x_src - x_i) by fused multiply-add,
+ *              in walk order. With ORRERY_FAST_TERM y is the hardware
+ *              approximation instead.
+ * Every traversal except the descend-together contrast gives bit-identical
+ * accelerations and interaction counts.
  *
  * Memory: every pointer named *_d or documented "device" is a CUDA device
  * pointer on the current device, owned by the caller. The library owns a
  * grow-only scratch workspace per device (released by orrery_bh_release).
  * Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
- * stream); each call blocks once at its end to read back a status word.
- * Calls are serialised by an internal lock; one call at a time per process.
+ * stream); each call blocks once at its end to read back a status word, so
+ * a call cannot be recorded into the caller's own stream capture (the
+ * library captures and replays its own CUDA graphs). Calls on one device
+ * are serialised by that device's lock; calls on different devices run
+ * concurrently.
  *
  * Errors: a negative status; on any non-zero status the outputs are undefined.
  */
