@@ -265,6 +265,28 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def accuracy_vs_direct(pos, mass, acc, eps, count=64, seed=20260811) -> dict:
+    """Worst and RMS relative error of the accelerations against the fp64
+    direct sum on a seeded sample of targets (numpy, after the timed region;
+    the pages' accuracy table measures the same two numbers)."""
+    rng = np.random.default_rng(seed)
+    n = pos.shape[0]
+    tgt = rng.choice(n, min(n, count), replace=False)
+    x = pos.astype(np.float64)
+    m = mass.astype(np.float64)
+    errs = []
+    for i in tgt:
+        d = x - x[i]
+        r2 = (d * d).sum(1) + float(eps) * float(eps)
+        w = m / (r2 * np.sqrt(r2))
+        w[i] = 0.0
+        ref = (w[:, None] * d).sum(0)
+        errs.append(np.linalg.norm(acc[i].astype(np.float64) - ref) / np.linalg.norm(ref))
+    errs = np.asarray(errs)
+    return {"vs": "fp64 direct sum", "targets": int(len(tgt)), "worst": float(errs.max()),
+            "rms": float(np.sqrt(np.mean(errs * errs)))}
+
+
 def cpu_baseline(pos, mass, params, seconds: float) -> dict:
     """The oracle as it stands on this host's cores: full tree build plus the
     walk of a sample of whole 32-target groups; scaled to interactions/s of a
@@ -534,6 +556,7 @@ def main():
             "ms_per_step": statistics.fmean(other_ms), "walk_ms": statistics.fmean(other_walk),
             "value": interactions / (statistics.fmean(other_ms) / 1000.0)},
         "comparison_traversals": comparison,
+        "accuracy": accuracy_vs_direct(pos_np, mass_np, h_out[0].numpy(), params["eps"]),
         "redundancy_width32": (comparison["coherent"]["visits_per_particle"] / vis_other)
         if "coherent" in comparison and args.traversal != "independent" else None,
     }
