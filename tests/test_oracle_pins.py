@@ -119,6 +119,30 @@ def test_plummer_recipe_properties():
     assert m.dtype == np.float32 and np.all(m == np.float32(1 / 20000))
 
 
+def ks_uniform(u, lo, hi):
+    """Kolmogorov-Smirnov distance of a sample from the uniform law on [lo, hi]."""
+    u = np.sort((np.asarray(u, np.float64) - lo) / (hi - lo))
+    k = np.arange(1, len(u) + 1) / len(u)
+    return max(np.max(k - u), np.max(u - (k - 1.0 / len(u))))
+
+
+def test_plummer_recipe_distributions():
+    # the mass fraction inside each particle's radius, X = r^3 / (1 + r^2)^1.5
+    # (the Plummer cumulative mass), is uniform on [0.001, 0.999]; the
+    # direction is isotropic: cos(polar) uniform on [-1, 1], azimuth uniform
+    n = 40000
+    pos, _ = plummer(n, 99)
+    x = pos.astype(np.float64)
+    r = np.linalg.norm(x, axis=1)
+    X = r ** 3 / (1.0 + r * r) ** 1.5
+    bound = 2.0 / math.sqrt(n)  # far above the 95 % KS quantile 1.36 / sqrt(n)
+    assert ks_uniform(X, 0.001, 0.999) < bound
+    assert ks_uniform(x[:, 2] / r, -1.0, 1.0) < bound
+    assert ks_uniform(np.arctan2(x[:, 1], x[:, 0]) % (2 * math.pi), 0.0, 2 * math.pi) < bound
+    # a generator that drew cos(polar) = u instead of 2u - 1 would fail
+    assert ks_uniform(np.abs(x[:, 2] / r), -1.0, 1.0) > 10 * bound
+
+
 # ---------------------------------------------------------------------------
 # steps 1-3: cube, keys, sort
 # ---------------------------------------------------------------------------
