@@ -74,13 +74,17 @@ k_build_levels(const uint64_t *__restrict__ K, int64_t n, int32_t cap,
     pstart[i] = (int32_t)s;
 }
 
-// Writes the nodes that start at each position: {escape, first, count, level},
-// the parent index, and counts children with an atomic add on the parent.
+// Writes the nodes that start at each position: their first particle and
+// level, the parent index (the first node's parent is the level-D cell found
+// by k_build_levels, every later one's is the node before it: the cells
+// starting at one position are nested), and counts children with an atomic
+// add on the parent. The cells' ends come from k_build_ends, one node per
+// thread, so no thread walks a chain of searches.
 __global__ void __launch_bounds__(kThreads)
-k_build_emit(const uint64_t *__restrict__ K, int64_t n, const int8_t *__restrict__ lev_d,
-             const uint8_t *__restrict__ ncount, const int32_t *__restrict__ pstart,
-             const uint32_t *__restrict__ node_start, int64_t max_nodes, int4 *__restrict__ meta,
-             int32_t *__restrict__ parent, int32_t *__restrict__ nchild, DeviceParams *P)
+k_build_emit(int64_t n, const int8_t *__restrict__ lev_d, const uint8_t *__restrict__ ncount,
+             const int32_t *__restrict__ pstart, const uint32_t *__restrict__ node_start,
+             int64_t max_nodes, int4 *__restrict__ meta, int32_t *__restrict__ parent,
+             int32_t *__restrict__ nchild, DeviceParams *P)
 {
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
@@ -91,7 +95,6 @@ k_build_emit(const uint64_t *__restrict__ K, int64_t n, const int8_t *__restrict
     }
     const int cnt = ncount[i];
     if (cnt == 0 || (int64_t)total > max_nodes) return;
-    const uint64_t key = K[i];
     const int D = lev_d[i];
     const int first_level = (i == 0) ? 0 : D + 1;
     const uint32_t base = node_start[i];
@@ -105,30 +108,48 @@ k_build_emit(const uint64_t *__restrict__ K, int64_t n, const int8_t *__restrict
             return;
         }
     }
-    int64_t hi = n;  // the cells starting at i are nested: each ends no later
     for (int j = 0; j < cnt; ++j) {
-        const int L = first_level + j;
         const int64_t k = (int64_t)base + j;
-        int64_t end = n;
-        if (L > 0) {
-            const uint64_t upper = key | ((1ull << (3 * (kLevels - L))) - 1ull);
-            int64_t lo = i + 1, h = hi;
-            while (lo < h) {
-                int64_t mid = (lo + h) >> 1;
-                if (K[mid] <= upper)
-                    lo = mid + 1;
-                else
-                    h = mid;
-            }
-            end = lo;
-        }
-        hi = end;
-        meta[k] = make_int4((int)node_start[end], (int)i, (int)(end - i), L);
+        meta[k] = make_int4(0, (int)i, 0, first_level + j);  // escape and count: k_build_ends
         parent[k] = par;
         if (par >= 0) atomicAdd(&nchild[par], 1);
         par = (int32_t)k;
     }
     atomicMax(&P->depth, first_level + cnt - 1);
+}
+
+// One thread per node: the end of its cell (the first position past the
+// keys that share the node's top L octal digits; a binary search over the
+// sorted keys), hence its particle count and escape index (the node index at
+// that position).
+__global__ void __launch_bounds__(kThreads)
+k_build_ends(const uint64_t *__restrict__ K, int64_t n, const uint32_t *__restrict__ node_start,
+             int64_t max_nodes, int4 *__restrict__ meta, DeviceParams *P)
+{
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t total = node_start[n];
+    if (k >= total || total > max_nodes) return;
+    const int4 m = meta[k];
+    const int64_t i = m.y;
+    const int L = m.w;
+    if (i < 0 || i >= n || L < 0 || L > kLevels) {
+        atomicOr(&P->status, kStatusInternal);
+        return;
+    }
+    int64_t end = n;
+    if (L > 0) {
+        const uint64_t upper = K[i] | ((1ull << (3 * (kLevels - L))) - 1ull);
+        int64_t lo = i + 1, hi = n;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi) >> 1;
+            if (K[mid] <= upper)
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        end = lo;
+    }
+    meta[k] = make_int4((int)node_start[end], (int)i, (int)(end - i), L);
 }
 
 // A node whose mass is not finite or whose CoM lies at 2^126 or beyond is
@@ -236,9 +257,12 @@ void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &
     launch_scan_u8(b.ncount, b.node_start, b.n + 1, b.scan_partial, st);
     cudaMemsetAsync(b.nchild, 0, sizeof(int32_t) * (size_t)b.max_nodes, st);
     k_build_emit<<<ceil_div(b.n, kThreads), kThreads, 0, st>>>(
-        keys_sorted, b.n, b.lev_d, b.ncount, b.pstart, b.node_start, b.max_nodes, b.meta,
-        b.parent, b.nchild, b.params);
-    g_launches += 1;
+        b.n, b.lev_d, b.ncount, b.pstart, b.node_start, b.max_nodes, b.meta, b.parent, b.nchild,
+        b.params);
+    // the node count is only known on the device: cover the bound
+    k_build_ends<<<ceil_div(b.max_nodes, kThreads), kThreads, 0, st>>>(
+        keys_sorted, b.n, b.node_start, b.max_nodes, b.meta, b.params);
+    g_launches += 2;
 }
 
 void launch_moments(const Buffers &b, cudaStream_t st)
