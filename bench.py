@@ -548,6 +548,7 @@ def main():
                     if len(step_ms) >= 2 else 0.0,
                     "wall_s_incl_flush": wall},
         "tree": {"num_nodes": phases[-1]["num_nodes"], "depth": phases[-1]["depth"]},
+        "interactions_per_s_walk": interactions / (walk_ms / 1000.0),
         "per_particle": {"interactions": interactions / n, "cells": pc_mean, "particles": pp_mean,
                          "visits": vis_mean, "visits_" + other: vis_other,
                          "redundancy": (vis_mean / vis_other) if args.traversal != "independent"
