@@ -360,6 +360,7 @@ GraphEntry *graph_for(Workspace &w, const GraphKey &key, const float *pos, const
         return nullptr;
     }
     prepare_sort();  // function attributes are set outside the capture
+    prepare_walk();
     const uint64_t before = g_launches.load();
     if (cudaStreamBeginCapture(w.capture_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
         cudaGetLastError();

@@ -100,6 +100,7 @@ void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *p
 int64_t scan_partial_count(int64_t count);
 int radix_blocks_for(int64_t n);
 void prepare_sort();  // sets the sort kernels' function attributes on this device
+void prepare_walk();  // sets the walk kernels' function attributes on this device
 int radix_bins();
 
 // --- small device helpers -------------------------------------------------

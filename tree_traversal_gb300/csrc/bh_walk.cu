@@ -45,6 +45,7 @@
 // a few ulp of monotone), every r2 is normal (so the fast term may use the
 // flush-to-zero hardware root), and the per-particle self comparison is
 // dropped.
+#include <atomic>
 #include <cfloat>
 #include <type_traits>
 
@@ -334,13 +335,23 @@ __device__ __forceinline__ void add_term2(const Sep2 &s, float m, bool use0, boo
     az = __ffma2_rn(f, s.dz, az);
 }
 
-// Lane l of warp w holds sorted targets 64w + l and 64w + 32 + l.
-template <bool kCount, bool kSelfFree, bool kFast>
-__device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, float4 *stage)
+// Shared-memory copies of everything a walk step reads, for small problems.
+struct LocalTree {
+    const WalkNode *nodes;  // [num_nodes]
+    const int *first;       // [num_nodes] first particle of each node
+    const float4 *ps;       // [n] sorted particles
+};
+
+// Lane l of warp w holds sorted targets 64w + l and 64w + 32 + l. kLocal:
+// nodes, first indices and leaf particles are read from the block's
+// shared-memory copies (loc) instead of global memory.
+template <bool kCount, bool kSelfFree, bool kFast, bool kLocal = false>
+__device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, float4 *stage,
+                                            LocalTree loc = LocalTree{})
 {
     constexpr unsigned kFull = 0xffffffffu;
     const int lane = threadIdx.x & 31;
-    const int base = a.t_begin + ((blockIdx.x * kThreads + threadIdx.x) >> 5) * 64;
+    const int base = a.t_begin + ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 64;
     const int t0 = base + lane, t1 = base + 32 + lane;
     const bool v0 = t0 < a.t_end, v1 = t1 < a.t_end;
     const float4 p0 = v0 ? __ldg(a.ps + t0) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -356,8 +367,8 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
     for (; steps <= num_nodes; ++steps) {
         const int k = __reduce_min_sync(kFull, min(next0, next1));
         if (k >= num_nodes) break;
-        const int4 w = __ldg(&a.wnode[k].w);
-        const float4 c = __ldg(&a.wnode[k].c);
+        const int4 w = kLocal ? loc.nodes[k].w : __ldg(&a.wnode[k].w);
+        const float4 c = kLocal ? loc.nodes[k].c : __ldg(&a.wnode[k].c);
         const bool act0 = next0 == k, act1 = next1 == k;
         const Sep2 s = separation2(c.x, c.y, c.z, nx, ny, nz);
         const float2 lim = __fmul2_rn(theta2, s.d2);
@@ -375,7 +386,7 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
         if (act0) next0 = acc0 ? w.x : w.y;
         if (act1) next1 = acc1 ? w.x : w.y;
         if (__any_sync(kFull, open0 || open1)) {
-            const int first = __ldg(&a.meta[k].y), count = w.z;
+            const int first = kLocal ? loc.first[k] : __ldg(&a.meta[k].y), count = w.z;
             if (first < 0 || first > a.n - count) {  // warp-uniform consistency check
                 if (lane == 0) atomicOr(&a.P->status, kStatusInternal);
                 break;
@@ -383,6 +394,17 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
             if (kCount) {
                 pp0 += open0 ? count - ((unsigned)(t0 - first) < (unsigned)count ? 1u : 0u) : 0u;
                 pp1 += open1 ? count - ((unsigned)(t1 - first) < (unsigned)count ? 1u : 0u) : 0u;
+            }
+            if (kLocal) {  // the particles are in shared memory already: read them as broadcasts
+                const int self0 = t0 - first, self1 = t1 - first;
+#pragma unroll 4
+                for (int j = 0; j < count; ++j) {
+                    const float4 q = loc.ps[first + j];
+                    const Sep2 sj = separation2(q.x, q.y, q.z, nx, ny, nz);
+                    add_term2<kFast, kSelfFree>(sj, q.w, open0 && (kSelfFree || j != self0),
+                                                open1 && (kSelfFree || j != self1), eps2, ax, ay, az);
+                }
+                continue;
             }
             for (int b = 0; b < count; b += 32) {
                 const int chunk = min(32, count - b);
@@ -417,6 +439,53 @@ __global__ void __launch_bounds__(kThreads) k_walk_paired(WalkArgs a)
         paired_walk<kCount, true, kFast>(a, num_nodes, stage);
     else
         paired_walk<kCount, false, kFast>(a, num_nodes, stage);
+}
+
+// Small problems: too few warps to hide the latency of the L2 reads every
+// step makes (the node, a leaf's first index, its particles), which then sets
+// the pace of the whole walk. Each block first copies the nodes, the leaves'
+// first indices and all sorted particles into shared memory (when they fit
+// in kLocalBytes; the node count is only known on the device), then walks
+// from there. Blocks of kLocalThreads spread the few warps over more SMs.
+constexpr int kLocalThreads = 64;
+constexpr int kLocalBytes = 200 * 1024;
+constexpr int64_t kLocalMaxTargets = 16384;
+constexpr int64_t kLocalMaxN = kLocalBytes / (int64_t)sizeof(float4);
+
+template <bool kCount, bool kFast>
+__global__ void __launch_bounds__(kLocalThreads) k_walk_paired_local(WalkArgs a)
+{
+    extern __shared__ __align__(16) unsigned char s_dyn[];
+    __shared__ float4 s_leaf[kLocalThreads / 32][32];
+    int num_nodes;
+    bool self_free;
+    if (!prologue<kFast>(a, num_nodes, self_free)) return;  // block-uniform
+    const int64_t need = (int64_t)num_nodes * (sizeof(WalkNode) + sizeof(int)) +
+                         (int64_t)a.n * sizeof(float4);
+    float4 *stage = s_leaf[threadIdx.x >> 5];
+    if (need > kLocalBytes) {  // block-uniform: walk from global memory
+        if (self_free)
+            paired_walk<kCount, true, kFast>(a, num_nodes, stage);
+        else
+            paired_walk<kCount, false, kFast>(a, num_nodes, stage);
+        return;
+    }
+    WalkNode *nodes = reinterpret_cast<WalkNode *>(s_dyn);
+    float4 *ps = reinterpret_cast<float4 *>(nodes + num_nodes);
+    int *first = reinterpret_cast<int *>(ps + a.n);
+    {
+        const int4 *src = reinterpret_cast<const int4 *>(a.wnode);
+        int4 *dst = reinterpret_cast<int4 *>(nodes);
+        for (int i = threadIdx.x; i < 2 * num_nodes; i += kLocalThreads) dst[i] = __ldg(src + i);
+        for (int i = threadIdx.x; i < a.n; i += kLocalThreads) ps[i] = __ldg(a.ps + i);
+        for (int i = threadIdx.x; i < num_nodes; i += kLocalThreads) first[i] = __ldg(&a.meta[i].y);
+    }
+    __syncthreads();
+    const LocalTree loc{nodes, first, ps};
+    if (self_free)
+        paired_walk<kCount, true, kFast, true>(a, num_nodes, stage, loc);
+    else
+        paired_walk<kCount, false, kFast, true>(a, num_nodes, stage, loc);
 }
 
 // The scheme the pages reject, kept as a measured contrast (ADR-0029,
@@ -562,11 +631,20 @@ void launch_kernels(int traversal, bool count, unsigned grid, const WalkArgs &a,
     case 1: coherent(std::integral_constant<int, 32>{}); break;
     case 2: coherent(std::integral_constant<int, 16>{}); break;
     case 3: {
-        const unsigned g = ceil_div(a.t_end - a.t_begin, (int64_t)kThreads * 2);  // 64 targets per warp
-        if (count)
-            k_walk_paired<true, kFast><<<g, kThreads, 0, st>>>(a);
-        else
-            k_walk_paired<false, kFast><<<g, kThreads, 0, st>>>(a);
+        const int64_t targets = a.t_end - a.t_begin;
+        if (targets <= kLocalMaxTargets && a.n <= kLocalMaxN) {
+            const unsigned g = ceil_div(targets, (int64_t)kLocalThreads * 2);
+            if (count)
+                k_walk_paired_local<true, kFast><<<g, kLocalThreads, kLocalBytes, st>>>(a);
+            else
+                k_walk_paired_local<false, kFast><<<g, kLocalThreads, kLocalBytes, st>>>(a);
+        } else {
+            const unsigned g = ceil_div(targets, (int64_t)kThreads * 2);  // 64 targets per warp
+            if (count)
+                k_walk_paired<true, kFast><<<g, kThreads, 0, st>>>(a);
+            else
+                k_walk_paired<false, kFast><<<g, kThreads, 0, st>>>(a);
+        }
         break;
     }
     case 4:
@@ -591,6 +669,21 @@ void launch_kernels(int traversal, bool count, unsigned grid, const WalkArgs &a,
 
 }  // namespace
 
+// The local walk's shared memory exceeds the default 48 KB: opted in once
+// per device, outside any stream capture.
+void prepare_walk()
+{
+    static std::atomic<bool> configured[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && configured[dev].load()) return;
+    cudaFuncSetAttribute(k_walk_paired_local<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalBytes);
+    cudaFuncSetAttribute(k_walk_paired_local<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalBytes);
+    cudaFuncSetAttribute(k_walk_paired_local<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalBytes);
+    cudaFuncSetAttribute(k_walk_paired_local<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalBytes);
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+}
+
 void launch_walk(int traversal_flags, float theta, float eps, const uint32_t *perm,
                  const Buffers &b, int64_t t_begin, int64_t t_end, float *acc, uint32_t *inter,
                  uint32_t *visits, cudaStream_t st)
@@ -614,6 +707,7 @@ void launch_walk(int traversal_flags, float theta, float eps, const uint32_t *pe
     a.inter = inter;
     a.visits = visits;
     const unsigned grid = ceil_div(t_end - t_begin, kThreads);
+    prepare_walk();
     if (fast)
         launch_kernels<true>(traversal, count, grid, a, st);
     else
