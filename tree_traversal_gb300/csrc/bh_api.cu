@@ -81,6 +81,10 @@ struct Workspace {
     // captured evaluations, replayed when a call repeats its arguments
     cudaStream_t capture_stream = nullptr;
     std::vector<GraphEntry> graphs;
+    // argument sets seen once and not captured yet: a graph is captured on
+    // the second call with the same arguments, so one-off calls (new output
+    // buffers every time) never pay for a capture they cannot reuse
+    std::vector<GraphKey> seen;
     uint64_t tick = 0;
 };
 
@@ -88,6 +92,7 @@ void drop_graphs(Workspace *w)
 {
     for (auto &g : w->graphs) cudaGraphExecDestroy(g.exec);
     w->graphs.clear();
+    w->seen.clear();
 }
 
 bool graphs_enabled()
@@ -353,6 +358,18 @@ GraphEntry *graph_for(Workspace &w, const GraphKey &key, const float *pos, const
             g.last_use = ++w.tick;
             return &g;
         }
+    bool repeat = false;
+    for (size_t i = 0; i < w.seen.size(); ++i)
+        if (w.seen[i] == key) {
+            repeat = true;
+            w.seen.erase(w.seen.begin() + (long)i);
+            break;
+        }
+    if (!repeat) {  // first sight: remember it, launch directly
+        if (w.seen.size() >= kGraphCache * 2) w.seen.erase(w.seen.begin());
+        w.seen.push_back(key);
+        return nullptr;
+    }
     if (!w.capture_stream &&
         cudaStreamCreateWithFlags(&w.capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
         cudaGetLastError();
