@@ -339,7 +339,7 @@ __device__ __forceinline__ void add_term2(const Sep2 &s, float m, bool use0, boo
 struct LocalTree {
     const WalkNode *nodes;  // [num_nodes]
     const int *first;       // [num_nodes] first particle of each node
-    const float4 *ps;       // [n] sorted particles
+    const float4 *ps;       // [n] sorted particles, or null: leaves read global memory
 };
 
 // Lane l of warp w holds sorted targets 64w + l and 64w + 32 + l. kLocal:
@@ -395,7 +395,7 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
                 pp0 += open0 ? count - ((unsigned)(t0 - first) < (unsigned)count ? 1u : 0u) : 0u;
                 pp1 += open1 ? count - ((unsigned)(t1 - first) < (unsigned)count ? 1u : 0u) : 0u;
             }
-            if (kLocal) {  // the particles are in shared memory already: read them as broadcasts
+            if (kLocal && loc.ps) {  // the particles are in shared memory: read them as broadcasts
                 const int self0 = t0 - first, self1 = t1 - first;
 #pragma unroll 4
                 for (int j = 0; j < count; ++j) {
@@ -441,29 +441,40 @@ __global__ void __launch_bounds__(kThreads) k_walk_paired(WalkArgs a)
         paired_walk<kCount, false, kFast>(a, num_nodes, stage);
 }
 
-// Small problems: too few warps to hide the latency of the L2 reads every
-// step makes (the node, a leaf's first index, its particles), which then sets
-// the pace of the whole walk. Each block first copies the nodes, the leaves'
-// first indices and all sorted particles into shared memory (when they fit
-// in kLocalBytes; the node count is only known on the device), then walks
-// from there. Blocks of kLocalThreads spread the few warps over more SMs.
+// Small and mid-size problems: too few warps to hide the latency of the L2
+// reads every step makes (the node, a leaf's first index, its particles),
+// which then sets the pace of the whole walk. Each block first copies into
+// shared memory the nodes and the leaves' first indices and, when they fit
+// too, all sorted particles (the node count is only known on the device, so
+// the fit is decided there), then walks from there. Up to kLocalMaxTargets
+// targets the blocks have kLocalThreads threads to spread the few warps over
+// more SMs; up to kLocalWaveTargets (one block of kThreads per SM) they have
+// kThreads, so one SM's warps share its L1 for the leaves read from global
+// memory. Above that the plain kernel runs: enough warps to hide latency.
 constexpr int kLocalThreads = 64;
 constexpr int kLocalBytes = 200 * 1024;
 constexpr int64_t kLocalMaxTargets = 16384;
 constexpr int64_t kLocalMaxN = kLocalBytes / (int64_t)sizeof(float4);
+constexpr int64_t kLocalWaveTargets = 152 * 2 * kThreads;
+// Above about 40 000 particles the nodes of a leaf-32 tree no longer fit
+// (about 0.13 nodes per particle, 36 bytes each), and a block that falls back
+// to global memory with this much shared memory reserved was measured slower
+// than the plain kernel (65 536 particles: 0.99 vs 0.82 ms).
+constexpr int64_t kLocalMidMaxN = 40000;
 
-template <bool kCount, bool kFast>
-__global__ void __launch_bounds__(kLocalThreads) k_walk_paired_local(WalkArgs a)
+template <int kBlock, bool kCount, bool kFast>
+__global__ void __launch_bounds__(kBlock) k_walk_paired_local(WalkArgs a)
 {
     extern __shared__ __align__(16) unsigned char s_dyn[];
-    __shared__ float4 s_leaf[kLocalThreads / 32][32];
+    __shared__ float4 s_leaf[kBlock / 32][32];
     int num_nodes;
     bool self_free;
     if (!prologue<kFast>(a, num_nodes, self_free)) return;  // block-uniform
-    const int64_t need = (int64_t)num_nodes * (sizeof(WalkNode) + sizeof(int)) +
-                         (int64_t)a.n * sizeof(float4);
+    const int64_t tree_bytes = (int64_t)num_nodes * (sizeof(WalkNode) + sizeof(int));
+    const int64_t ps_offset = (tree_bytes + 15) & ~int64_t(15);
+    const bool with_ps = ps_offset + (int64_t)a.n * (int64_t)sizeof(float4) <= kLocalBytes;  // block-uniform
     float4 *stage = s_leaf[threadIdx.x >> 5];
-    if (need > kLocalBytes) {  // block-uniform: walk from global memory
+    if (tree_bytes > kLocalBytes) {  // block-uniform: walk from global memory
         if (self_free)
             paired_walk<kCount, true, kFast>(a, num_nodes, stage);
         else
@@ -471,14 +482,15 @@ __global__ void __launch_bounds__(kLocalThreads) k_walk_paired_local(WalkArgs a)
         return;
     }
     WalkNode *nodes = reinterpret_cast<WalkNode *>(s_dyn);
-    float4 *ps = reinterpret_cast<float4 *>(nodes + num_nodes);
-    int *first = reinterpret_cast<int *>(ps + a.n);
+    int *first = reinterpret_cast<int *>(nodes + num_nodes);
+    float4 *ps = with_ps ? reinterpret_cast<float4 *>(s_dyn + ps_offset) : nullptr;
     {
         const int4 *src = reinterpret_cast<const int4 *>(a.wnode);
         int4 *dst = reinterpret_cast<int4 *>(nodes);
-        for (int i = threadIdx.x; i < 2 * num_nodes; i += kLocalThreads) dst[i] = __ldg(src + i);
-        for (int i = threadIdx.x; i < a.n; i += kLocalThreads) ps[i] = __ldg(a.ps + i);
-        for (int i = threadIdx.x; i < num_nodes; i += kLocalThreads) first[i] = __ldg(&a.meta[i].y);
+        for (int i = threadIdx.x; i < 2 * num_nodes; i += kBlock) dst[i] = __ldg(src + i);
+        for (int i = threadIdx.x; i < num_nodes; i += kBlock) first[i] = __ldg(&a.meta[i].y);
+        if (with_ps)
+            for (int i = threadIdx.x; i < a.n; i += kBlock) ps[i] = __ldg(a.ps + i);
     }
     __syncthreads();
     const LocalTree loc{nodes, first, ps};
@@ -635,9 +647,15 @@ void launch_kernels(int traversal, bool count, unsigned grid, const WalkArgs &a,
         if (targets <= kLocalMaxTargets && a.n <= kLocalMaxN) {
             const unsigned g = ceil_div(targets, (int64_t)kLocalThreads * 2);
             if (count)
-                k_walk_paired_local<true, kFast><<<g, kLocalThreads, kLocalBytes, st>>>(a);
+                k_walk_paired_local<kLocalThreads, true, kFast><<<g, kLocalThreads, kLocalBytes, st>>>(a);
             else
-                k_walk_paired_local<false, kFast><<<g, kLocalThreads, kLocalBytes, st>>>(a);
+                k_walk_paired_local<kLocalThreads, false, kFast><<<g, kLocalThreads, kLocalBytes, st>>>(a);
+        } else if (targets <= kLocalWaveTargets && a.n <= kLocalMidMaxN) {
+            const unsigned g = ceil_div(targets, (int64_t)kThreads * 2);
+            if (count)
+                k_walk_paired_local<kThreads, true, kFast><<<g, kThreads, kLocalBytes, st>>>(a);
+            else
+                k_walk_paired_local<kThreads, false, kFast><<<g, kThreads, kLocalBytes, st>>>(a);
         } else {
             const unsigned g = ceil_div(targets, (int64_t)kThreads * 2);  // 64 targets per warp
             if (count)
@@ -677,10 +695,17 @@ void prepare_walk()
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && configured[dev].load()) return;
-    cudaFuncSetAttribute(k_walk_paired_local<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalBytes);
-    cudaFuncSetAttribute(k_walk_paired_local<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalBytes);
-    cudaFuncSetAttribute(k_walk_paired_local<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalBytes);
-    cudaFuncSetAttribute(k_walk_paired_local<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalBytes);
+    auto opt_in = [](const void *f) {
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalBytes);
+    };
+    opt_in((const void *)k_walk_paired_local<kLocalThreads, true, true>);
+    opt_in((const void *)k_walk_paired_local<kLocalThreads, true, false>);
+    opt_in((const void *)k_walk_paired_local<kLocalThreads, false, true>);
+    opt_in((const void *)k_walk_paired_local<kLocalThreads, false, false>);
+    opt_in((const void *)k_walk_paired_local<kThreads, true, true>);
+    opt_in((const void *)k_walk_paired_local<kThreads, true, false>);
+    opt_in((const void *)k_walk_paired_local<kThreads, false, true>);
+    opt_in((const void *)k_walk_paired_local<kThreads, false, false>);
     if (dev >= 0 && dev < 64) configured[dev] = true;
 }
 
