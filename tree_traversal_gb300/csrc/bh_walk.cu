@@ -179,6 +179,13 @@ __device__ __forceinline__ bool prologue(const WalkArgs &a, int &num_nodes, bool
     return s_state[0] == 0;
 }
 
+// Shared-memory copies of everything a walk step reads, for small problems.
+struct LocalTree {
+    const WalkNode *nodes;  // [num_nodes]
+    const int *first;       // [num_nodes] first particle of each node
+    const float4 *ps;       // [n] sorted particles, or null: leaves read global memory
+};
+
 // One coherence group = W consecutive sorted targets sharing one node index,
 // one target per lane. W = 16: half a warp per group (two groups per warp,
 // each advancing on its own, like the pages' sub-group width of 16); W = 32:
@@ -193,15 +200,16 @@ __device__ __forceinline__ bool prologue(const WalkArgs &a, int &num_nodes, bool
 // of an accepted ancestor of k, which is never below escape(k) -- so the
 // ballot form visits exactly the same union; it is kept to measure the cost
 // of the two instructions against each other.
-template <int W, bool kCount, bool kSelfFree, bool kBallot, bool kFast>
-__device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, float4 *stage)
+template <int W, bool kCount, bool kSelfFree, bool kBallot, bool kFast, bool kLocal = false>
+__device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, float4 *stage,
+                                              LocalTree loc = LocalTree{})
 {
     static_assert(W == 16 || W == 32, "one target per lane");
     constexpr int G = W;
     const int lane = threadIdx.x & 31;
     const int glane = lane & (G - 1);
     const unsigned gmask = (G == 32) ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
-    const int tgt = a.t_begin + blockIdx.x * kThreads + threadIdx.x;
+    const int tgt = a.t_begin + blockIdx.x * blockDim.x + threadIdx.x;
     const bool valid = tgt < a.t_end;
     const float4 xi = valid ? __ldg(a.ps + tgt) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     int next = valid ? 0 : num_nodes;
@@ -212,8 +220,8 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
     for (; steps <= num_nodes; ++steps) {
         const int k = kBallot ? kb : __reduce_min_sync(gmask, next);
         if (k >= num_nodes) break;
-        const int4 w = __ldg(&a.wnode[k].w);
-        const float4 c = __ldg(&a.wnode[k].c);
+        const int4 w = kLocal ? loc.nodes[k].w : __ldg(&a.wnode[k].w);
+        const float4 c = kLocal ? loc.nodes[k].c : __ldg(&a.wnode[k].c);
         bool open = false, descend = false;
         if (next == k) {
             const float dx = __fsub_rn(c.x, xi.x);
@@ -232,12 +240,22 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
         }
         if (kBallot) kb = __any_sync(gmask, descend) ? k + 1 : w.x;
         if (__any_sync(gmask, open)) {
-            const int first = __ldg(&a.meta[k].y), count = w.z;
+            const int first = kLocal ? loc.first[k] : __ldg(&a.meta[k].y), count = w.z;
             if (first < 0 || first > a.n - count) {  // group-uniform consistency check
                 if (glane == 0) atomicOr(&a.P->status, kStatusInternal);
                 break;
             }
             if (kCount && open) pp += count - ((unsigned)(tgt - first) < (unsigned)count ? 1u : 0u);
+            if (kLocal && loc.ps) {  // the particles are in shared memory: read them as broadcasts
+                if (open) {
+                    const int self = tgt - first;
+#pragma unroll 4
+                    for (int j = 0; j < count; ++j)
+                        if (kSelfFree || j != self)
+                            particle_term<kFast, kSelfFree>(loc.ps[first + j], xi, a.eps2, ax, ay, az);
+                }
+                continue;
+            }
             for (int b = 0; b < count; b += G) {
                 const int chunk = min(G, count - b);
                 if (glane < chunk) stage[glane] = __ldg(a.ps + first + b + glane);
@@ -335,12 +353,6 @@ __device__ __forceinline__ void add_term2(const Sep2 &s, float m, bool use0, boo
     az = __ffma2_rn(f, s.dz, az);
 }
 
-// Shared-memory copies of everything a walk step reads, for small problems.
-struct LocalTree {
-    const WalkNode *nodes;  // [num_nodes]
-    const int *first;       // [num_nodes] first particle of each node
-    const float4 *ps;       // [n] sorted particles, or null: leaves read global memory
-};
 
 // Lane l of warp w holds sorted targets 64w + l and 64w + 32 + l. kLocal:
 // nodes, first indices and leaf particles are read from the block's
@@ -462,8 +474,18 @@ constexpr int64_t kLocalWaveTargets = 152 * 2 * kThreads;
 // than the plain kernel (65 536 particles: 0.99 vs 0.82 ms).
 constexpr int64_t kLocalMidMaxN = 40000;
 
-template <int kBlock, bool kCount, bool kFast>
-__global__ void __launch_bounds__(kBlock) k_walk_paired_local(WalkArgs a)
+// W = 64: the packed walk; W = 32 or 16: the one-target-per-lane walk.
+template <int W, bool kCount, bool kSelfFree, bool kFast, bool kLocal>
+__device__ __forceinline__ void any_walk(const WalkArgs &a, int num_nodes, float4 *stage, LocalTree loc)
+{
+    if constexpr (W == 64)
+        paired_walk<kCount, kSelfFree, kFast, kLocal>(a, num_nodes, stage, loc);
+    else
+        coherent_walk<W, kCount, kSelfFree, false, kFast, kLocal>(a, num_nodes, stage, loc);
+}
+
+template <int kBlock, int W, bool kCount, bool kFast>
+__global__ void __launch_bounds__(kBlock) k_walk_local(WalkArgs a)
 {
     extern __shared__ __align__(16) unsigned char s_dyn[];
     __shared__ float4 s_leaf[kBlock / 32][32];
@@ -473,12 +495,13 @@ __global__ void __launch_bounds__(kBlock) k_walk_paired_local(WalkArgs a)
     const int64_t tree_bytes = (int64_t)num_nodes * (sizeof(WalkNode) + sizeof(int));
     const int64_t ps_offset = (tree_bytes + 15) & ~int64_t(15);
     const bool with_ps = ps_offset + (int64_t)a.n * (int64_t)sizeof(float4) <= kLocalBytes;  // block-uniform
-    float4 *stage = s_leaf[threadIdx.x >> 5];
+    // the group's slots of the per-warp leaf stage (a half warp at W = 16)
+    float4 *stage = &s_leaf[threadIdx.x >> 5][(threadIdx.x & 31) & ~((W < 32 ? W : 32) - 1)];
     if (tree_bytes > kLocalBytes) {  // block-uniform: walk from global memory
         if (self_free)
-            paired_walk<kCount, true, kFast>(a, num_nodes, stage);
+            any_walk<W, kCount, true, kFast, false>(a, num_nodes, stage, LocalTree{});
         else
-            paired_walk<kCount, false, kFast>(a, num_nodes, stage);
+            any_walk<W, kCount, false, kFast, false>(a, num_nodes, stage, LocalTree{});
         return;
     }
     WalkNode *nodes = reinterpret_cast<WalkNode *>(s_dyn);
@@ -495,9 +518,9 @@ __global__ void __launch_bounds__(kBlock) k_walk_paired_local(WalkArgs a)
     __syncthreads();
     const LocalTree loc{nodes, first, ps};
     if (self_free)
-        paired_walk<kCount, true, kFast, true>(a, num_nodes, stage, loc);
+        any_walk<W, kCount, true, kFast, true>(a, num_nodes, stage, loc);
     else
-        paired_walk<kCount, false, kFast, true>(a, num_nodes, stage, loc);
+        any_walk<W, kCount, false, kFast, true>(a, num_nodes, stage, loc);
 }
 
 // The scheme the pages reject, kept as a measured contrast (ADR-0029,
@@ -632,8 +655,33 @@ __global__ void __launch_bounds__(kThreads) k_walk_independent(WalkArgs a)
 template <bool kFast>
 void launch_kernels(int traversal, bool count, unsigned grid, const WalkArgs &a, cudaStream_t st)
 {
+    const int64_t targets = a.t_end - a.t_begin;
+    // the shared-memory walks for small and mid-size problems (see above);
+    // returns false when the plain kernels should run
+    auto local = [&](auto wtag) -> bool {
+        constexpr int W = decltype(wtag)::value;
+        constexpr int per_thread = W == 64 ? 2 : 1;
+        if (targets <= kLocalMaxTargets && a.n <= kLocalMaxN) {
+            const unsigned g = ceil_div(targets, (int64_t)kLocalThreads * per_thread);
+            if (count)
+                k_walk_local<kLocalThreads, W, true, kFast><<<g, kLocalThreads, kLocalBytes, st>>>(a);
+            else
+                k_walk_local<kLocalThreads, W, false, kFast><<<g, kLocalThreads, kLocalBytes, st>>>(a);
+            return true;
+        }
+        if (targets <= kLocalWaveTargets && a.n <= kLocalMidMaxN) {
+            const unsigned g = ceil_div(targets, (int64_t)kThreads * per_thread);
+            if (count)
+                k_walk_local<kThreads, W, true, kFast><<<g, kThreads, kLocalBytes, st>>>(a);
+            else
+                k_walk_local<kThreads, W, false, kFast><<<g, kThreads, kLocalBytes, st>>>(a);
+            return true;
+        }
+        return false;
+    };
     auto coherent = [&](auto wtag) {
         constexpr int W = decltype(wtag)::value;
+        if (local(wtag)) return;
         if (count)
             k_walk_coherent<W, true, false, kFast><<<grid, kThreads, 0, st>>>(a);
         else
@@ -643,26 +691,12 @@ void launch_kernels(int traversal, bool count, unsigned grid, const WalkArgs &a,
     case 1: coherent(std::integral_constant<int, 32>{}); break;
     case 2: coherent(std::integral_constant<int, 16>{}); break;
     case 3: {
-        const int64_t targets = a.t_end - a.t_begin;
-        if (targets <= kLocalMaxTargets && a.n <= kLocalMaxN) {
-            const unsigned g = ceil_div(targets, (int64_t)kLocalThreads * 2);
-            if (count)
-                k_walk_paired_local<kLocalThreads, true, kFast><<<g, kLocalThreads, kLocalBytes, st>>>(a);
-            else
-                k_walk_paired_local<kLocalThreads, false, kFast><<<g, kLocalThreads, kLocalBytes, st>>>(a);
-        } else if (targets <= kLocalWaveTargets && a.n <= kLocalMidMaxN) {
-            const unsigned g = ceil_div(targets, (int64_t)kThreads * 2);
-            if (count)
-                k_walk_paired_local<kThreads, true, kFast><<<g, kThreads, kLocalBytes, st>>>(a);
-            else
-                k_walk_paired_local<kThreads, false, kFast><<<g, kThreads, kLocalBytes, st>>>(a);
-        } else {
-            const unsigned g = ceil_div(targets, (int64_t)kThreads * 2);  // 64 targets per warp
-            if (count)
-                k_walk_paired<true, kFast><<<g, kThreads, 0, st>>>(a);
-            else
-                k_walk_paired<false, kFast><<<g, kThreads, 0, st>>>(a);
-        }
+        if (local(std::integral_constant<int, 64>{})) break;
+        const unsigned g = ceil_div(targets, (int64_t)kThreads * 2);  // 64 targets per warp
+        if (count)
+            k_walk_paired<true, kFast><<<g, kThreads, 0, st>>>(a);
+        else
+            k_walk_paired<false, kFast><<<g, kThreads, 0, st>>>(a);
         break;
     }
     case 4:
@@ -698,14 +732,21 @@ void prepare_walk()
     auto opt_in = [](const void *f) {
         cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalBytes);
     };
-    opt_in((const void *)k_walk_paired_local<kLocalThreads, true, true>);
-    opt_in((const void *)k_walk_paired_local<kLocalThreads, true, false>);
-    opt_in((const void *)k_walk_paired_local<kLocalThreads, false, true>);
-    opt_in((const void *)k_walk_paired_local<kLocalThreads, false, false>);
-    opt_in((const void *)k_walk_paired_local<kThreads, true, true>);
-    opt_in((const void *)k_walk_paired_local<kThreads, true, false>);
-    opt_in((const void *)k_walk_paired_local<kThreads, false, true>);
-    opt_in((const void *)k_walk_paired_local<kThreads, false, false>);
+    auto each = [&](auto btag, auto wtag) {
+        constexpr int B = decltype(btag)::value, W = decltype(wtag)::value;
+        opt_in((const void *)k_walk_local<B, W, true, true>);
+        opt_in((const void *)k_walk_local<B, W, true, false>);
+        opt_in((const void *)k_walk_local<B, W, false, true>);
+        opt_in((const void *)k_walk_local<B, W, false, false>);
+    };
+    using L = std::integral_constant<int, kLocalThreads>;
+    using T = std::integral_constant<int, kThreads>;
+    each(L{}, std::integral_constant<int, 64>{});
+    each(L{}, std::integral_constant<int, 32>{});
+    each(L{}, std::integral_constant<int, 16>{});
+    each(T{}, std::integral_constant<int, 64>{});
+    each(T{}, std::integral_constant<int, 32>{});
+    each(T{}, std::integral_constant<int, 16>{});
     if (dev >= 0 && dev < 64) configured[dev] = true;
 }
 
