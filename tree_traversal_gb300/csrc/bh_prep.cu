@@ -250,27 +250,32 @@ k_scan_partials(uint32_t *__restrict__ partial, int64_t parts)
     }
 }
 
-template <typename T>
+// kItems per thread; partial == null: a single block scans everything.
+template <typename T, int kItems>
 __global__ void __launch_bounds__(kScanThreads)
 k_scan_down(const T *__restrict__ in, uint32_t *__restrict__ out, int64_t count,
             const uint32_t *__restrict__ partial)
 {
-    int64_t base = (int64_t)blockIdx.x * kScanTile + threadIdx.x * kScanItems;
-    uint32_t v[kScanItems];
+    int64_t base = (int64_t)blockIdx.x * kScanThreads * kItems + threadIdx.x * kItems;
+    uint32_t v[kItems];
     uint32_t s = 0;
 #pragma unroll
-    for (int j = 0; j < kScanItems; ++j) {
+    for (int j = 0; j < kItems; ++j) {
         v[j] = (base + j < count) ? in[base + j] : 0u;
         s += v[j];
     }
     uint32_t total;
-    uint32_t run = block_exclusive_scan(s, total) + partial[blockIdx.x];
+    uint32_t run = block_exclusive_scan(s, total) + (partial ? partial[blockIdx.x] : 0u);
 #pragma unroll
-    for (int j = 0; j < kScanItems; ++j) {
+    for (int j = 0; j < kItems; ++j) {
         if (base + j < count) out[base + j] = run;
         run += v[j];
     }
 }
+
+// Up to this many entries one block scans in one launch instead of three.
+constexpr int kScanSingleItems = 32;
+constexpr int64_t kScanSingle = (int64_t)kScanThreads * kScanSingleItems;  // 8192
 
 }  // namespace
 
@@ -280,10 +285,15 @@ template <typename T>
 static void scan_exclusive(const T *in, uint32_t *out, int64_t count, uint32_t *partial,
                            cudaStream_t st)
 {
+    if (count <= kScanSingle) {
+        k_scan_down<T, kScanSingleItems><<<1, kScanThreads, 0, st>>>(in, out, count, nullptr);
+        g_launches += 1;
+        return;
+    }
     int64_t parts = scan_partial_count(count);
     k_scan_reduce<T><<<(unsigned)parts, kScanThreads, 0, st>>>(in, count, partial);
     k_scan_partials<<<1, kScanThreads, 0, st>>>(partial, parts);
-    k_scan_down<T><<<(unsigned)parts, kScanThreads, 0, st>>>(in, out, count, partial);
+    k_scan_down<T, kScanItems><<<(unsigned)parts, kScanThreads, 0, st>>>(in, out, count, partial);
     g_launches += 3;
 }
 
