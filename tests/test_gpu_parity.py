@@ -527,7 +527,7 @@ def _random_config(seed):
     return pos, mass, cap, theta, eps, trav
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", list(range(24)) + list(range(100, 124)))
 def test_random_configurations_bit_exact(tt, seed):
     pos, mass, cap, theta, eps, trav = _random_config(seed)
     T = oracle.Tree(pos, mass, cap)
