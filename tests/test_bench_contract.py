@@ -30,7 +30,7 @@ def test_bench_line_has_the_contract_keys():
     assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
     assert d["config"]["workload"] == "plummer_16384" and "model" not in d["config"]
-    assert d["gpu_launches"] >= 3 * 20  # every phase of every timed step is one of ours
+    assert d["gpu_launches"] >= 3 * 12  # every phase of every timed step is one of ours
     r = d["roofline"]
     assert r["bound"] == "alu" and r["unit"] == "TFLOP/s" and 0 < r["frac"] < 1.5
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9

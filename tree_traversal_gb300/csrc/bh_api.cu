@@ -137,7 +137,7 @@ size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
     };
     b.n = n;
     b.max_nodes = nodes;
-    b.radix_blocks = radix_blocks_for(n);
+    b.sort_tiles = sort_tiles_for(n);
     b.bbox_blocks = bbox_blocks_for(n);
     const size_t n1 = (size_t)n + 1;
     b.bbox_partial = (float *)take(sizeof(float) * 8 * (size_t)b.bbox_blocks);
@@ -146,8 +146,8 @@ size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
     b.keys_b = (uint64_t *)take(sizeof(uint64_t) * (size_t)n);
     b.idx_a = (uint32_t *)take(sizeof(uint32_t) * (size_t)n);
     b.idx_b = (uint32_t *)take(sizeof(uint32_t) * (size_t)n);
-    b.radix_hist = (uint32_t *)take(sizeof(uint32_t) * radix_bins() * (size_t)b.radix_blocks);
-    b.radix_total = (uint32_t *)take(sizeof(uint32_t) * radix_bins());
+    b.sort_ctl = (uint32_t *)take(sizeof(uint32_t) * (size_t)sort_ctl_words());
+    b.sort_look = (uint32_t *)take(sizeof(uint32_t) * (size_t)sort_look_words(n));
     b.ps = (float4 *)take(sizeof(float4) * (size_t)n);
     b.lev_d = (int8_t *)take(n1);
     b.lev_w = (int8_t *)take(n1);

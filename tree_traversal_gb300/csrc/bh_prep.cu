@@ -1,13 +1,14 @@
 // bh_prep.cu -- the data-movement phases before the tree: bounding cube,
-// Morton keys, gather into tree order, and a device-wide exclusive scan used
-// by the build. (The scatter back to the caller's order is fused into the
-// walk's epilogue.)
+// gather into tree order, and a device-wide exclusive scan used by the
+// build. (The Morton keys are made in bh_sort.cu, together with the digit
+// counts of their sort; the scatter back to the caller's order is fused into
+// the walk's epilogue.)
 //
 // Pages: "sycl_tree_solver.hpp" (Detailed Description, "Where the tree comes
 // from": particles are copied into the tree's sorted order before the walk
 // and the accelerations scattered back to the caller's order afterwards).
-// The bounding cube and the 21-bit key follow the workload definition that
-// accompanies the pages (a quantised bounding cube, 21 bits per axis).
+// The bounding cube follows the workload definition that accompanies the
+// pages (a quantised bounding cube, 21 bits per axis).
 #include <math.h>
 
 #include "bh_common.cuh"
@@ -135,41 +136,6 @@ k_bbox_final(const float *__restrict__ partial, int blocks, DeviceParams *P)
     P->status = bad ? kStatusNonFinite : 0;
     P->num_nodes = 0;
     P->depth = 0;
-}
-
-// Spreads the low 21 bits of v so that bit b lands at bit 3b.
-__device__ __forceinline__ uint64_t spread3(uint32_t v)
-{
-    uint64_t x = v & 0x1fffffu;
-    x = (x | (x << 32)) & 0x001f00000000ffffull;
-    x = (x | (x << 16)) & 0x001f0000ff0000ffull;
-    x = (x | (x << 8)) & 0x100f00f00f00f00full;
-    x = (x | (x << 4)) & 0x10c30c30c30c30c3ull;
-    x = (x | (x << 2)) & 0x1249249249249249ull;
-    return x;
-}
-
-// q = min(floor(fl(fl(x - lo) * inv)), 2^21 - 1)
-__device__ __forceinline__ uint32_t quantise(float x, float lo, float inv)
-{
-    float t = __fmul_rn(__fsub_rn(x, lo), inv);
-    if (!(t >= 0.0f)) t = 0.0f;
-    if (t >= 2097151.0f) return 2097151u;
-    return (uint32_t)t;  // truncation is floor for t >= 0
-}
-
-// a2: 63-bit Morton key per particle, x the high bit of each level's triple.
-__global__ void __launch_bounds__(256)
-k_morton(const float *__restrict__ pos, int64_t n, const DeviceParams *__restrict__ P,
-         uint64_t *__restrict__ keys)
-{
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const float inv = P->inv;
-    uint32_t qx = quantise(__ldg(pos + 3 * i + 0), P->lo[0], inv);
-    uint32_t qy = quantise(__ldg(pos + 3 * i + 1), P->lo[1], inv);
-    uint32_t qz = quantise(__ldg(pos + 3 * i + 2), P->lo[2], inv);
-    keys[i] = (spread3(qx) << 2) | (spread3(qy) << 1) | spread3(qz);
 }
 
 // a4: sorted particles {x, y, z, m}.
@@ -308,12 +274,6 @@ void launch_bbox(const float *pos, const float *mass, const Buffers &b, cudaStre
     k_bbox_partial<<<b.bbox_blocks, kBBoxThreads, 0, st>>>(pos, mass, b.n, b.bbox_partial);
     k_bbox_final<<<1, kBBoxThreads, 0, st>>>(b.bbox_partial, b.bbox_blocks, b.params);
     g_launches += 2;
-}
-
-void launch_morton(const float *pos, const Buffers &b, cudaStream_t st)
-{
-    k_morton<<<ceil_div(b.n, 256), 256, 0, st>>>(pos, b.n, b.params, b.keys_a);
-    g_launches += 1;
 }
 
 void launch_gather(const float *pos, const float *mass, const uint32_t *perm, const Buffers &b,

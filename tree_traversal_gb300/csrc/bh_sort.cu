@@ -1,61 +1,162 @@
-// bh_sort.cu -- a3: stable least-significant-digit radix sort of (key, index).
+// bh_sort.cu -- a2 Morton keys and a3 their stable least-significant-digit
+// radix sort of (key, index).
 //
 // The pages name the host Morton sort as the limit of their solver (orrery:
 // docs/performance/sycl_tree.md, the five findings and "Where one evaluation
 // goes": 40-46 per cent of every evaluation) and a device radix sort as the
-// first thing to do about it. Seven passes of 9 bits cover the 63-bit keys.
-// Each pass is three launches with no inter-block waiting: per-tile digit
-// counts, a per-digit scan over tiles, and a stable scatter. The scatter
-// ranks every key of its 2048-key tile (each warp walks a contiguous 256-key
-// span 32 keys at a time, ranking equal digits with a match-any vote), puts
-// the tile in digit order in shared memory, and then writes each digit's run
-// to its global slot with consecutive threads on consecutive addresses.
+// first thing to do about it. The 21-bit quantisation per axis follows the
+// workload definition that accompanies the pages (a quantised bounding cube,
+// 21 bits per axis). Seven passes of 9 bits cover the 63-bit keys.
+//
+// The key kernel also counts the digits of all seven passes at once (seven
+// 512-bin histograms), so every pass is a single launch in the manner of the
+// published "Onesweep" radix sort (Adinets and Merrill, 2022) with its
+// decoupled look-back (Merrill and Garland, 2016): a block takes the next
+// 4096-key tile by ticket, counts its digits, publishes the counts, and adds
+// up the counts of the tiles before it by reading their published words
+// backwards until it meets a tile that has already published its inclusive
+// prefix. A block only ever waits for tiles with smaller tickets, which are
+// already running, so every wait ends; each is still bounded, and a wait
+// that runs out flags an internal error instead of spinning on. The tile is
+// then ranked (each warp walks a contiguous 256-key span 32 keys at a time,
+// finding the lanes with equal digits by one vote per digit bit), put in
+// digit order in shared memory, and each digit's run is written to its
+// global slot with consecutive threads on consecutive addresses.
+#include <cuda/atomic>
+
 #include "bh_common.cuh"
 
 namespace obh {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kItems = 8;                       // per lane
-constexpr int kTile = kThreads * kItems;        // 2048 keys per block
+constexpr int kTile = kThreads * kItems;        // 4096 keys per block
 constexpr int kWarpSpan = 32 * kItems;          // 256 consecutive keys per warp
 constexpr int kBits = 9;
 constexpr int kBins = 1 << kBits;               // 512 digits
 constexpr int kPasses = 7;                      // 7 x 9 = 63 key bits
 constexpr int kBinsPerThread = kBins / kThreads;
 
-// dynamic shared memory of the scatter: digit counters and the reordered tile
-struct ScatterSmem {
-    uint32_t cnt[kWarps][kBins];  // per-warp digit counts, then offsets
-    uint32_t base[kBins];         // global start of each digit's run for this tile
-    uint32_t loc[kBins];          // start of each digit's run inside the tile
-    uint32_t warp_sum[kWarps];
-    uint64_t key[kTile];
-    uint32_t val[kTile];
-};
+// Control words of one sort, cleared before the key kernel: the digit counts
+// of every pass, then one tile ticket per pass.
+constexpr int kCtlCounts = kPasses * kBins;
+constexpr int kCtlWords = kCtlCounts + 8;
+
+// A look-back word: bit 31 set = the inclusive count of the digit over this
+// tile and all before it (at most 2^30, the largest n); bit 30 set = this
+// tile's own count only (at most 4096); zero = not yet published.
+constexpr uint32_t kLookInclusive = 0x80000000u;
+constexpr uint32_t kLookTileOnly = 0x40000000u;
+constexpr int kLookSpins = 1 << 20;  // polls of an unpublished word before giving up
+constexpr int kLookWindow = 4;       // earlier tiles' words read at once
+
+// Spreads the low 21 bits of v so that bit b lands at bit 3b.
+__device__ __forceinline__ uint64_t spread3(uint32_t v)
+{
+    uint64_t x = v & 0x1fffffu;
+    x = (x | (x << 32)) & 0x001f00000000ffffull;
+    x = (x | (x << 16)) & 0x001f0000ff0000ffull;
+    x = (x | (x << 8)) & 0x100f00f00f00f00full;
+    x = (x | (x << 4)) & 0x10c30c30c30c30c3ull;
+    x = (x | (x << 2)) & 0x1249249249249249ull;
+    return x;
+}
+
+// q = min(floor(fl(fl(x - lo) * inv)), 2^21 - 1)
+__device__ __forceinline__ uint32_t quantise(float x, float lo, float inv)
+{
+    float t = __fmul_rn(__fsub_rn(x, lo), inv);
+    if (!(t >= 0.0f)) t = 0.0f;
+    if (t >= 2097151.0f) return 2097151u;
+    return (uint32_t)t;  // truncation is floor for t >= 0
+}
+
+// 63-bit Morton key of particle i, x the high bit of each level's triple.
+__device__ __forceinline__ uint64_t morton_key(const float *__restrict__ pos, int64_t i,
+                                               const float lo[3], float inv)
+{
+    const uint32_t qx = quantise(__ldg(pos + 3 * i + 0), lo[0], inv);
+    const uint32_t qy = quantise(__ldg(pos + 3 * i + 1), lo[1], inv);
+    const uint32_t qz = quantise(__ldg(pos + 3 * i + 2), lo[2], inv);
+    return (spread3(qx) << 2) | (spread3(qy) << 1) | spread3(qz);
+}
 
 __device__ __forceinline__ uint32_t digit_of(uint64_t key, int shift)
 {
     return (uint32_t)((key >> shift) & (kBins - 1));
 }
 
-__global__ void __launch_bounds__(kThreads)
-k_radix_hist(const uint64_t *__restrict__ keys, int64_t n, int shift,
-             uint32_t *__restrict__ hist, int nblocks)
+// The lanes of this warp holding a valid key with this lane's digit: one vote
+// per digit bit. (A match-any vote gives the same set, but its cost grows
+// with the number of distinct digits in the warp: measured at about 1 000
+// cycles per 32 random 9-bit digits, against a few dozen for the votes.)
+__device__ __forceinline__ unsigned digit_peers(uint32_t dig, bool valid)
 {
-    __shared__ uint32_t h[kBins];
-    for (int d = threadIdx.x; d < kBins; d += kThreads) h[d] = 0;
-    __syncthreads();
-    int64_t base = (int64_t)blockIdx.x * kTile;
-#pragma unroll 4
-    for (int it = 0; it < kItems; ++it) {
-        int64_t e = base + it * kThreads + threadIdx.x;
-        if (e < n) atomicAdd(&h[digit_of(keys[e], shift)], 1u);
+    unsigned peers = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+    for (int b = 0; b < kBits; ++b) {
+        const bool bit = (dig >> b) & 1u;
+        const unsigned vote = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? vote : ~vote;
     }
+    return peers;
+}
+
+// Rank of this lane's key among the warp's keys with the same digit, counting
+// the keys of earlier rounds in cnt[digit] (updated here for the next round).
+__device__ __forceinline__ uint32_t warp_rank(uint32_t *cnt, uint32_t dig, bool valid)
+{
+    const unsigned lane_lt = (1u << (threadIdx.x & 31)) - 1u;
+    const unsigned peers = digit_peers(dig, valid);
+    const uint32_t before = valid ? cnt[dig] : 0u;
+    __syncwarp();
+    if (valid && (threadIdx.x & 31) == __ffs(peers) - 1) cnt[dig] = before + __popc(peers);
+    __syncwarp();
+    return before + __popc(peers & lane_lt);
+}
+
+// Keys only (the single-block sort counts its own digits).
+__global__ void __launch_bounds__(256)
+k_morton(const float *__restrict__ pos, int64_t n, const DeviceParams *__restrict__ P,
+         uint64_t *__restrict__ keys)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float lo[3] = {P->lo[0], P->lo[1], P->lo[2]};
+    keys[i] = morton_key(pos, i, lo, P->inv);
+}
+
+// Keys and the digit counts of all seven passes. Each block counts its keys
+// in shared memory and adds its histograms to the global ones; the grid also
+// clears the look-back words of the first pass.
+constexpr int kCountThreads = 512;
+constexpr int kCountKeysPerThread = 16;
+constexpr int kCountMaxBlocks = 2 * 152;
+
+__global__ void __launch_bounds__(kCountThreads)
+k_keys_count(const float *__restrict__ pos, int64_t n, const DeviceParams *__restrict__ P,
+             uint64_t *__restrict__ keys, uint32_t *__restrict__ counts,
+             uint32_t *__restrict__ look0, int64_t look_words)
+{
+    __shared__ uint32_t h[kCtlCounts];
+    for (int i = threadIdx.x; i < kCtlCounts; i += kCountThreads) h[i] = 0;
     __syncthreads();
-    for (int d = threadIdx.x; d < kBins; d += kThreads)
-        hist[(int64_t)d * nblocks + blockIdx.x] = h[d];
+    const float lo[3] = {P->lo[0], P->lo[1], P->lo[2]};
+    const float inv = P->inv;
+    const int64_t stride = (int64_t)gridDim.x * kCountThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kCountThreads + threadIdx.x; i < n; i += stride) {
+        const uint64_t key = morton_key(pos, i, lo, inv);
+        keys[i] = key;
+#pragma unroll
+        for (int p = 0; p < kPasses; ++p) atomicAdd(&h[p * kBins + digit_of(key, kBits * p)], 1u);
+    }
+    for (int64_t i = (int64_t)blockIdx.x * kCountThreads + threadIdx.x; i < look_words; i += stride)
+        look0[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < kCtlCounts; i += kCountThreads)
+        if (h[i]) atomicAdd(&counts[i], h[i]);
 }
 
 // Block-wide exclusive scan of one value per thread; also returns the total.
@@ -80,94 +181,163 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *warp_sum, u
     return before + x - v;
 }
 
-// One block per digit: exclusive scan of that digit's tile counts, in place.
-__global__ void __launch_bounds__(kThreads)
-k_radix_scan(uint32_t *__restrict__ hist, int nblocks, uint32_t *__restrict__ total)
+
+// dynamic shared memory of one pass: digit counters and the reordered tile
+struct PassSmem {
+    uint32_t cnt[kWarps][kBins];  // per-warp digit counts, then offsets
+    uint32_t base[kBins];         // global start of each digit's run for this tile
+    uint32_t loc[kBins];          // start of each digit's run inside the tile
+    uint32_t warp_sum[kWarps];
+    uint32_t tile;                // this block's ticket = its tile
+    uint64_t key[kTile];
+    uint32_t val[kTile];
+};
+
+// Look-back words are read and written as device-scope relaxed atomics: each
+// word carries its whole meaning, so no other memory needs ordering with it.
+__device__ __forceinline__ uint32_t look_load(uint32_t *p)
 {
-    __shared__ uint32_t warp_sum[kWarps];
-    uint32_t *row = hist + (int64_t)blockIdx.x * nblocks;
-    uint32_t carry = 0;
-    for (int base = 0; base < nblocks; base += kThreads) {
-        int i = base + threadIdx.x;
-        uint32_t v = (i < nblocks) ? row[i] : 0u;
-        uint32_t all;
-        uint32_t ex = block_scan(v, warp_sum, all);
-        if (i < nblocks) row[i] = carry + ex;
-        carry += all;
-    }
-    if (threadIdx.x == 0) total[blockIdx.x] = carry;
+    return cuda::atomic_ref<uint32_t, cuda::thread_scope_device>(*p).load(cuda::memory_order_relaxed);
 }
 
+__device__ __forceinline__ void look_store(uint32_t *p, uint32_t v)
+{
+    cuda::atomic_ref<uint32_t, cuda::thread_scope_device>(*p).store(v, cuda::memory_order_relaxed);
+}
+
+// One pass over the tile of this block's ticket. counts: the pass's digit
+// totals; ticket: the pass's tile counter (zero on entry); look: the pass's
+// look-back words [tiles][kBins] (zero on entry); look_next: the next pass's
+// words, whose row for this tile is cleared here (null on the last pass).
 __global__ void __launch_bounds__(kThreads)
-k_radix_scatter(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
-                uint64_t *__restrict__ kout, uint32_t *__restrict__ vout, int64_t n, int shift,
-                const uint32_t *__restrict__ hist, const uint32_t *__restrict__ total,
-                int nblocks, int first_pass, int *status)
+k_onesweep(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
+           uint64_t *__restrict__ kout, uint32_t *__restrict__ vout, int64_t n, int pass,
+           const uint32_t *__restrict__ counts, uint32_t *ticket, uint32_t *look,
+           uint32_t *look_next, int tiles, int *status)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    ScatterSmem &S = *reinterpret_cast<ScatterSmem *>(smem_raw);
+    PassSmem &S = *reinterpret_cast<PassSmem *>(smem_raw);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned lt = (1u << lane) - 1u;
-    const int64_t tile0 = (int64_t)blockIdx.x * kTile;
-    const int tile_n = (n - tile0 < (int64_t)kTile) ? (int)(n - tile0) : kTile;
+    const int shift = kBits * pass;
+    if (threadIdx.x == 0) S.tile = atomicAdd(ticket, 1u);
+    for (int d = threadIdx.x; d < kBins; d += kThreads)
+        for (int w = 0; w < kWarps; ++w) S.cnt[w][d] = 0;
 
-    // global start of each digit = exclusive scan of the digit totals, plus
-    // this tile's offset within the digit
+    // global start of each digit: exclusive scan of the pass's digit totals
+    uint32_t start[kBinsPerThread];
     {
         uint32_t v[kBinsPerThread], sum = 0;
 #pragma unroll
         for (int q = 0; q < kBinsPerThread; ++q) {
-            v[q] = total[threadIdx.x * kBinsPerThread + q];
+            v[q] = counts[threadIdx.x * kBinsPerThread + q];
             sum += v[q];
         }
         uint32_t all;
-        uint32_t run = block_scan(sum, S.warp_sum, all);
+        uint32_t run = block_scan(sum, S.warp_sum, all);  // its barriers also publish S.tile
 #pragma unroll
         for (int q = 0; q < kBinsPerThread; ++q) {
-            const int d = threadIdx.x * kBinsPerThread + q;
-            S.base[d] = run + hist[(int64_t)d * nblocks + blockIdx.x];
+            start[q] = run;
             run += v[q];
         }
-        for (int d = threadIdx.x; d < kBins; d += kThreads)
-            for (int w = 0; w < kWarps; ++w) S.cnt[w][d] = 0;
     }
-    __syncthreads();
+    const int tile = (int)S.tile;
+    if (tile >= tiles) {  // block-uniform; cannot happen with one block per tile
+        if (threadIdx.x == 0) atomicOr(status, kStatusInternal);
+        return;
+    }
+    if (look_next)
+        for (int d = threadIdx.x; d < kBins; d += kThreads) look_next[(int64_t)tile * kBins + d] = 0;
+    const int64_t tile0 = (int64_t)tile * kTile;
+    const int tile_n = (n - tile0 < (int64_t)kTile) ? (int)(n - tile0) : kTile;
 
-    // phase A: per-warp digit counts, spans walked in order
+    // phase A: per-warp digit counts and each key's rank inside its warp's
+    // run of the digit (one byte per round: a warp holds 256 keys), spans
+    // walked in order
     const int span = warp * kWarpSpan;
     uint64_t key[kItems];
     uint32_t val[kItems];
-    uint32_t dig[kItems];
+    uint32_t rank[kItems / 4] = {};
 #pragma unroll
     for (int r = 0; r < kItems; ++r) {
         const int e = span + r * 32 + lane;
         const bool ok = e < tile_n;
         key[r] = ok ? kin[tile0 + e] : 0ull;
-        val[r] = ok ? (first_pass ? (uint32_t)(tile0 + e) : vin[tile0 + e]) : 0u;
-        dig[r] = ok ? digit_of(key[r], shift) : (uint32_t)kBins;
-        const unsigned peers = __match_any_sync(0xffffffffu, dig[r]);
-        const int leader = __ffs(peers) - 1;
-        if (lane == leader && dig[r] < (uint32_t)kBins) S.cnt[warp][dig[r]] += __popc(peers);
-        __syncwarp();
+        val[r] = ok ? (pass == 0 ? (uint32_t)(tile0 + e) : vin[tile0 + e]) : 0u;
+    }
+#pragma unroll
+    for (int r = 0; r < kItems; ++r) {
+        const bool ok = span + r * 32 + lane < tile_n;
+        rank[r / 4] |= warp_rank(S.cnt[warp], digit_of(key[r], shift), ok) << (8 * (r % 4));
     }
     __syncthreads();
 
-    // per digit: offsets of each warp's first key inside the digit's run, and
-    // the start of each digit's run inside the tile
-    {
-        uint32_t c[kBinsPerThread], sum = 0;
+    // per digit: offsets of each warp's first key inside the tile's run, and
+    // the tile's count, published at once
+    uint32_t c[kBinsPerThread];
+    uint32_t *row = look + (int64_t)tile * kBins;
 #pragma unroll
-        for (int q = 0; q < kBinsPerThread; ++q) {
-            const int d = threadIdx.x * kBinsPerThread + q;
-            uint32_t run = 0;
-            for (int w = 0; w < kWarps; ++w) {
-                const uint32_t x = S.cnt[w][d];
-                S.cnt[w][d] = run;
-                run += x;
-            }
-            c[q] = run;
-            sum += run;
+    for (int q = 0; q < kBinsPerThread; ++q) {
+        const int d = threadIdx.x * kBinsPerThread + q;
+        uint32_t run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const uint32_t x = S.cnt[w][d];
+            S.cnt[w][d] = run;
+            run += x;
         }
+        c[q] = run;
+        look_store(row + d, (tile == 0 ? kLookInclusive : kLookTileOnly) | run);
+    }
+
+    // look-back: the count of each digit over all earlier tiles, reading the
+    // words of kLookWindow tiles at once and adding them nearest first up to
+    // the first inclusive one; an unpublished word ends the window and is
+    // read again after a growing pause
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) {
+        const int d = threadIdx.x * kBinsPerThread + q;
+        uint32_t before = 0;
+        if (tile > 0) {
+            int spins = 0;
+            unsigned pause = 32;
+            for (int j = tile - 1; j >= 0;) {
+                uint32_t s[kLookWindow];
+#pragma unroll
+                for (int u = 0; u < kLookWindow; ++u)  // past tile 0: an inclusive zero
+                    s[u] = j - u >= 0 ? look_load(look + (int64_t)(j - u) * kBins + d) : kLookInclusive;
+                int used = 0;
+                bool found = false;
+#pragma unroll
+                for (int u = 0; u < kLookWindow; ++u) {
+                    if (found || used < u) break;
+                    if (s[u] & kLookInclusive) {
+                        before += s[u] & ~kLookInclusive;
+                        found = true;
+                    } else if (s[u] & kLookTileOnly) {
+                        before += s[u] & ~kLookTileOnly;
+                        ++used;
+                    }
+                }
+                if (found) break;
+                j -= used;
+                if (used == 0) {  // tile j has not published yet
+                    if (++spins > kLookSpins) {  // it never did: give up, flagged
+                        atomicOr(status, kStatusInternal);
+                        break;
+                    }
+                    __nanosleep(pause);
+                    pause = pause < 1024 ? 2 * pause : pause;
+                }
+            }
+            look_store(row + d, kLookInclusive | (before + c[q]));
+        }
+        S.base[d] = start[q] + before;
+    }
+
+    // start of each digit's run inside the tile
+    {
+        uint32_t sum = 0;
+#pragma unroll
+        for (int q = 0; q < kBinsPerThread; ++q) sum += c[q];
         uint32_t all;
         uint32_t run = block_scan(sum, S.warp_sum, all);
 #pragma unroll
@@ -181,10 +351,9 @@ k_radix_scatter(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ v
     // phase B: place every key at its stable position inside the tile
 #pragma unroll
     for (int r = 0; r < kItems; ++r) {
-        const unsigned peers = __match_any_sync(0xffffffffu, dig[r]);
-        const int leader = __ffs(peers) - 1;
-        if (dig[r] < (uint32_t)kBins) {
-            const uint32_t p = S.loc[dig[r]] + S.cnt[warp][dig[r]] + __popc(peers & lt);
+        if (span + r * 32 + lane < tile_n) {
+            const uint32_t d = digit_of(key[r], shift);
+            const uint32_t p = S.loc[d] + S.cnt[warp][d] + ((rank[r / 4] >> (8 * (r % 4))) & 0xffu);
             if (p < (uint32_t)tile_n) {
                 S.key[p] = key[r];
                 S.val[p] = val[r];
@@ -192,9 +361,6 @@ k_radix_scatter(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ v
                 atomicOr(status, kStatusInternal);
             }
         }
-        __syncwarp();
-        if (lane == leader && dig[r] < (uint32_t)kBins) S.cnt[warp][dig[r]] += __popc(peers);
-        __syncwarp();
     }
     __syncthreads();
 
@@ -213,18 +379,18 @@ k_radix_scatter(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ v
 }
 
 // Up to 4096 keys: the whole sort in one block, all seven passes in
-// shared memory. Each pass ranks the keys exactly as the scatter above (per-
-// warp digit counts with match-any votes, spans and rounds walked in key
-// order, so equal digits keep their order), writes every key to its rank in
-// shared memory and reads its new keys back. One launch instead of 21: at
-// these sizes the sort is bound by launch latency, not by work.
+// shared memory. Each pass ranks the keys exactly as k_onesweep (per-
+// warp digit counts and ranks from digit-bit votes, spans and rounds walked
+// in key order, so equal digits keep their order), writes every key to its rank in
+// shared memory and reads its new keys back. One launch instead of eight:
+// at these sizes the sort is bound by launch latency, not by work.
 constexpr int kSmallThreads = 512;
 constexpr int kSmallWarps = kSmallThreads / 32;
 constexpr int kSmallItems = 8;                           // rounds per lane at most
 // 4096 keys at most: the cost grows with the rounds per lane (about 6 us per
 // round over the seven passes, scattering keys into shared memory; measured
-// 31 / 68 us at 1024 / 4096 keys against 76 / 101 us for the multi-block
-// passes), so beyond 4096 keys it would no longer win.
+// 31 / 68 us at 1024 / 4096 keys), so beyond 4096 keys it would no longer
+// win.
 constexpr int kSmallN = kSmallThreads * kSmallItems;     // 4096
 
 struct SmallSortSmem {
@@ -264,7 +430,6 @@ k_radix_sort_small(const uint64_t *__restrict__ kin, uint64_t *__restrict__ kout
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SmallSortSmem &S = *reinterpret_cast<SmallSortSmem *>(smem_raw);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned lt = (1u << lane) - 1u;
     // each warp takes a contiguous span of rounds * 32 keys, just enough to
     // cover n; rounds walk the span in key order (round-major, then lane)
     const int rounds = (n + kSmallThreads - 1) / kSmallThreads;
@@ -281,15 +446,12 @@ k_radix_sort_small(const uint64_t *__restrict__ kin, uint64_t *__restrict__ kout
         const int shift = kBits * pass;
         for (int i = threadIdx.x; i < kSmallWarps * kBins; i += kSmallThreads) (&S.cnt[0][0])[i] = 0;
         __syncthreads();
-        uint32_t dig[kSmallItems];
+        uint32_t rank[kSmallItems / 4] = {};
 #pragma unroll
-        for (int r = 0; r < kSmallItems; ++r) {  // per-warp digit counts
-            const int e = span + r * 32 + lane;
-            dig[r] = (r < rounds && e < n) ? digit_of(key[r], shift) : (uint32_t)kBins;
-            if (r >= rounds) continue;  // warp-uniform
-            const unsigned peers = __match_any_sync(0xffffffffu, dig[r]);
-            if (lane == __ffs(peers) - 1 && dig[r] < (uint32_t)kBins) S.cnt[warp][dig[r]] += __popc(peers);
-            __syncwarp();
+        for (int r = 0; r < kSmallItems; ++r) {  // per-warp digit counts and ranks
+            if (r >= rounds) break;  // warp-uniform
+            const bool ok = span + r * 32 + lane < n;
+            rank[r / 4] |= warp_rank(S.cnt[warp], digit_of(key[r], shift), ok) << (8 * (r % 4));
         }
         __syncthreads();
         {  // thread d owns digit d: offsets of each warp's first key in the run
@@ -307,9 +469,9 @@ k_radix_sort_small(const uint64_t *__restrict__ kin, uint64_t *__restrict__ kout
 #pragma unroll
         for (int r = 0; r < kSmallItems; ++r) {  // every key to its stable rank
             if (r >= rounds) break;  // warp-uniform
-            const unsigned peers = __match_any_sync(0xffffffffu, dig[r]);
-            if (dig[r] < (uint32_t)kBins) {
-                const uint32_t p = S.loc[dig[r]] + S.cnt[warp][dig[r]] + __popc(peers & lt);
+            if (span + r * 32 + lane < n) {
+                const uint32_t d = digit_of(key[r], shift);
+                const uint32_t p = S.loc[d] + S.cnt[warp][d] + ((rank[r / 4] >> (8 * (r % 4))) & 0xffu);
                 if (p < (uint32_t)n) {
                     S.key[p] = key[r];
                     S.val[p] = val[r];
@@ -317,9 +479,6 @@ k_radix_sort_small(const uint64_t *__restrict__ kin, uint64_t *__restrict__ kout
                     atomicOr(status, kStatusInternal);
                 }
             }
-            __syncwarp();
-            if (lane == __ffs(peers) - 1 && dig[r] < (uint32_t)kBins) S.cnt[warp][dig[r]] += __popc(peers);
-            __syncwarp();
         }
         __syncthreads();
 #pragma unroll
@@ -342,30 +501,47 @@ k_radix_sort_small(const uint64_t *__restrict__ kin, uint64_t *__restrict__ kout
     }
 }
 
+
 }  // namespace
 
-// Sorts b.keys_a (filled by the key phase) with the original indices as
-// values. Seven passes: the result lands in keys_b / idx_b.
 void prepare_sort()
 {
     static std::atomic<bool> configured[64];  // the opt-in is set once per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !configured[dev].load()) {
-        cudaFuncSetAttribute(k_radix_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(ScatterSmem));
+        cudaFuncSetAttribute(k_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(PassSmem));
         cudaFuncSetAttribute(k_radix_sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(SmallSortSmem));
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
 }
 
+// a2: the keys into b.keys_a; above the single-block size also the digit
+// counts of every pass, with the sort's control words cleared first.
+void launch_morton(const float *pos, const Buffers &b, cudaStream_t st)
+{
+    if (b.n <= kSmallN) {
+        k_morton<<<ceil_div(b.n, 256), 256, 0, st>>>(pos, b.n, b.params, b.keys_a);
+        g_launches += 1;
+        return;
+    }
+    cudaMemsetAsync(b.sort_ctl, 0, sizeof(uint32_t) * kCtlWords, st);
+    int64_t blocks = ((int64_t)b.n + kCountThreads * kCountKeysPerThread - 1) /
+                     (kCountThreads * kCountKeysPerThread);
+    if (blocks > kCountMaxBlocks) blocks = kCountMaxBlocks;
+    k_keys_count<<<(unsigned)blocks, kCountThreads, 0, st>>>(
+        pos, b.n, b.params, b.keys_a, b.sort_ctl, b.sort_look, (int64_t)b.sort_tiles * kBins);
+    g_launches += 1;
+}
+
+// a3: sorts b.keys_a (from launch_morton) with the original indices as
+// values; returns where the sorted keys and the permutation landed.
 void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint32_t **perm)
 {
-    const int nb = b.radix_blocks;
-    const size_t smem = sizeof(ScatterSmem);
     prepare_sort();
-    if (b.n <= kSmallN) {  // one block, one launch; the result lands where the passes' would
+    if (b.n <= kSmallN) {  // one block, one launch
         k_radix_sort_small<<<1, kSmallThreads, sizeof(SmallSortSmem), st>>>(
             b.keys_a, b.keys_b, b.idx_b, (int)b.n, &b.params->status);
         g_launches += 1;
@@ -373,16 +549,17 @@ void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint
         *perm = b.idx_b;
         return;
     }
+    const int tiles = b.sort_tiles;
+    const int64_t look_words = (int64_t)tiles * kBins;
     uint64_t *kin = b.keys_a, *kout = b.keys_b;
     uint32_t *vin = b.idx_a, *vout = b.idx_b;
     for (int p = 0; p < kPasses; ++p) {
-        const int shift = kBits * p;
-        k_radix_hist<<<nb, kThreads, 0, st>>>(kin, b.n, shift, b.radix_hist, nb);
-        k_radix_scan<<<kBins, kThreads, 0, st>>>(b.radix_hist, nb, b.radix_total);
-        k_radix_scatter<<<nb, kThreads, smem, st>>>(kin, vin, kout, vout, b.n, shift,
-                                                    b.radix_hist, b.radix_total, nb, p == 0,
-                                                    &b.params->status);
-        g_launches += 3;
+        uint32_t *look = b.sort_look + (p & 1) * look_words;
+        uint32_t *look_next = p + 1 < kPasses ? b.sort_look + ((p + 1) & 1) * look_words : nullptr;
+        k_onesweep<<<tiles, kThreads, sizeof(PassSmem), st>>>(
+            kin, vin, kout, vout, b.n, p, b.sort_ctl + p * kBins, b.sort_ctl + kCtlCounts + p,
+            look, look_next, tiles, &b.params->status);
+        g_launches += 1;
         uint64_t *tk = kin;
         kin = kout;
         kout = tk;
@@ -394,8 +571,10 @@ void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint
     *perm = vin;
 }
 
-int radix_blocks_for(int64_t n) { return (int)((n + kTile - 1) / kTile); }
+int sort_tiles_for(int64_t n) { return (int)((n + kTile - 1) / kTile); }
 
-int radix_bins() { return kBins; }
+int64_t sort_look_words(int64_t n) { return 2 * (int64_t)sort_tiles_for(n) * kBins; }
+
+int sort_ctl_words() { return kCtlWords; }
 
 }  // namespace obh
