@@ -497,6 +497,9 @@ def main():
                           args.traversal, out=h_out, device=device, fast_term=fast)
         e2e_ms.append(1000.0 * (time.perf_counter() - t1))
     e2e_host = tt.last_timings()
+    # measured FP32 FMA rate (long independent chains on every SM), beside
+    # the nominal peak: untimed, after everything above
+    fma = tt.fp32_fma_rate(device)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -532,7 +535,12 @@ def main():
                      "frac_at_sampled_clock": (achieved / (peak_tflops * csum["sm_mhz"] / clk))
                      if csum["sm_mhz"] else None,
                      "frac_incl_acceptance": (flops_inter + FLOPS_PER_VISIT * vis_ind * n)
-                     / (walk_ms / 1000.0) / 1e12 / peak_tflops},
+                     / (walk_ms / 1000.0) / 1e12 / peak_tflops,
+                     "peak_measured_fma": {"scalar": fma["scalar"], "packed": fma["packed"],
+                                           "unit": "TFLOP/s", "sm_mhz": fma["sm_mhz"],
+                                           "lanes_per_sm_clock": fma["scalar"] * 1e12 / 2
+                                           / (sms * fma["sm_mhz"] * 1e6) if fma["sm_mhz"] else None},
+                     "frac_of_measured_fma": achieved / max(fma["scalar"], fma["packed"])},
         "cpu_baseline": None if cb is None else
         {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "walk_interactions_per_s_1_thread",
                              "walk_interactions_per_s_all_threads")},

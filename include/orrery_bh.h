@@ -255,6 +255,21 @@ int orrery_direct_forces(const float *pos_d, const float *mass_d, int64_t n, flo
  * Returns -1 for invalid arguments. */
 int64_t orrery_bh_max_nodes(int64_t n, int32_t leaf_cap);
 
+/* The FP32 fused multiply-add rate this GPU delivers, measured: long
+ * independent FMA chains on every SM, scalar (FFMA) and packed (FFMA2, two
+ * FMAs per lane per instruction, the form the walk's arithmetic uses), each
+ * timed with CUDA events over one launch after an untimed one (about 15 ms
+ * each on a GB300). The walk is bound by plain FP32 arithmetic, so this is
+ * its measured roofline denominator beside the nominal SMs x 128 lanes x 2
+ * flops x clock. Work is enqueued on `stream` (a cudaStream_t, NULL for the
+ * default stream) and the call blocks until it is done; calls are serialised.
+ *   tflops_scalar, tflops_packed: host outputs, TFLOP/s (an FMA = 2 flops).
+ *   sm_mhz: host output or NULL: the SM clock during the scalar probe (each
+ *           block's clock cycles over the launch's elapsed time, median).
+ * Returns ORRERY_OK, ORRERY_EINVAL (a null rate output) or ORRERY_ECUDA. */
+int orrery_fp32_fma_rate(double *tflops_scalar, double *tflops_packed, double *sm_mhz,
+                         void *stream);
+
 /* Copies the phase timings of the last successful evaluation on this process. */
 int orrery_bh_last_timings(orrery_bh_timings *out);
 

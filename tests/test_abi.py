@@ -40,7 +40,7 @@ def test_header_declares_the_entry_points():
     for want in ("orrery_bh_forces", "orrery_bh_forces_host", "orrery_bh_tree",
                  "orrery_direct_forces",
                  "orrery_bh_max_nodes", "orrery_bh_last_timings", "orrery_bh_kernel_launches",
-                 "orrery_bh_strerror", "orrery_bh_release"):
+                 "orrery_bh_strerror", "orrery_bh_release", "orrery_fp32_fma_rate"):
         assert want in names
 
 

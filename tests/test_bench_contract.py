@@ -34,6 +34,9 @@ def test_bench_line_has_the_contract_keys():
     r = d["roofline"]
     assert r["bound"] == "alu" and r["unit"] == "TFLOP/s" and 0 < r["frac"] < 1.5
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    assert r["peak_measured_fma"]["scalar"] > 0 and r["peak_measured_fma"]["packed"] > 0
+    assert r["peak_measured_fma"]["sm_mhz"] > 0
+    assert 0 < r["frac_of_measured_fma"] < 1.5
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
     e = d["e2e"]

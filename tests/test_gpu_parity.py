@@ -687,3 +687,19 @@ def test_concurrent_callers_on_one_device(tt):
     for i, got in results.items():
         assert torch.equal(got[0].view(torch.int32), ref[0].view(torch.int32))
         assert torch.equal(got[1], ref[1])
+
+
+@pytest.mark.gpu
+def test_fp32_fma_rate_is_within_the_pipes_nominal_range(tt):
+    """The measured FMA rate (the walk's roofline denominator) lies between a
+    quarter of the nominal rate at 1 GHz and the nominal rate at 2.2 GHz, for
+    scalar and packed chains alike."""
+    r = tt.fp32_fma_rate()
+    scalar, packed = r["scalar"], r["packed"]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    per_ghz = sms * 128 * 2 * 1e9 / 1e12  # TFLOP/s per GHz of SM clock
+    for rate in (scalar, packed):
+        assert 0.25 * per_ghz < rate < 2.2 * per_ghz, r
+    assert 0.5 < packed / scalar < 2.5
+    # the rate per clock cannot exceed the 128 lanes of an SM
+    assert 300 < r["sm_mhz"] < 2200 and scalar / (per_ghz * r["sm_mhz"] / 1000) <= 1.02, r

@@ -15,6 +15,7 @@ from .bh import (  # noqa: F401
     bh_forces_host,
     bh_tree,
     direct_forces,
+    fp32_fma_rate,
     kernel_launches,
     last_timings,
     max_nodes,

@@ -98,6 +98,8 @@ def load(path: str | None = None):
         lib.orrery_bh_max_nodes.restype = i64
         lib.orrery_bh_last_timings.argtypes = [ctypes.POINTER(Timings)]
         lib.orrery_bh_last_timings.restype = ctypes.c_int
+        lib.orrery_fp32_fma_rate.argtypes = [ctypes.POINTER(ctypes.c_double)] * 3 + [P]
+        lib.orrery_fp32_fma_rate.restype = ctypes.c_int
         lib.orrery_bh_kernel_launches.argtypes = []
         lib.orrery_bh_kernel_launches.restype = ctypes.c_uint64
         lib.orrery_bh_strerror.argtypes = [ctypes.c_int]

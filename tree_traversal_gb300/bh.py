@@ -198,6 +198,20 @@ def last_timings() -> dict:
     return t.as_dict()
 
 
+def fp32_fma_rate(device=None) -> dict:
+    """Measured FP32 FMA rate of the GPU, long independent chains on every SM,
+    on the current stream: {"scalar": TFLOP/s of FFMA, "packed": TFLOP/s of
+    FFMA2, "sm_mhz": the SM clock during the scalar probe}."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    scalar, packed, mhz = ctypes.c_double(0.0), ctypes.c_double(0.0), ctypes.c_double(0.0)
+    with torch.cuda.device(dev):
+        rc = _lib.load().orrery_fp32_fma_rate(ctypes.byref(scalar), ctypes.byref(packed),
+                                               ctypes.byref(mhz), _stream_handle(dev))
+    if rc != _lib.OK:
+        raise _lib.OrreryError(rc, "orrery_fp32_fma_rate")
+    return {"scalar": float(scalar.value), "packed": float(packed.value), "sm_mhz": float(mhz.value)}
+
+
 def kernel_launches() -> int:
     return int(_lib.load().orrery_bh_kernel_launches())
 
