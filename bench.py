@@ -45,6 +45,9 @@ def parse():
     p.add_argument("--steps", type=int, default=11)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--workload", default="plummer_1048576")
+    p.add_argument("--theta", type=float, default=None,
+                   help="opening angle instead of the workload's (the two-sphere set is swept "
+                        "over 0.3, 0.5 and 0.7)")
     p.add_argument("--traversal", default="coherent64",
                    choices=["coherent", "coherent16", "coherent64", "ballot", "together",
                             "independent"])
@@ -339,6 +342,8 @@ def run_reference(args, rank: int, world: int) -> None:
     if rank != 0:
         return
     pos, mass, params = workload(args.workload)
+    if args.theta is not None:
+        params["theta"] = args.theta
     times, vals = [], []
     cb = None
     for step in range(args.warmup + args.steps):
@@ -396,6 +401,8 @@ def main():
     tt.load()
 
     pos_np, mass_np, params = workload(args.workload)
+    if args.theta is not None:
+        params["theta"] = args.theta
     n = pos_np.shape[0]
     pos = torch.from_numpy(pos_np).to(device)
     mass = torch.from_numpy(mass_np).to(device)
