@@ -121,10 +121,18 @@ k_build_emit(int64_t n, const int8_t *__restrict__ lev_d, const uint8_t *__restr
 // One thread per node: the end of its cell (the first position past the
 // keys that share the node's top L octal digits; a binary search over the
 // sorted keys), hence its particle count and escape index (the node index at
-// that position).
+// that position), and the node's walk record {escape, the node a target that
+// does not accept it goes to next (escape for a leaf, which it opens; k + 1
+// for an internal node, which it enters), leaf count (0 for an internal
+// node), bits of (side 2^-level)^2}. Every node k < num_nodes gets its record
+// here, and every record's next nodes are checked to lie in (k, num_nodes]:
+// so a walk's node index strictly increases and every walk ends within
+// num_nodes steps (an escape outside that range is flagged and replaced by
+// num_nodes).
 __global__ void __launch_bounds__(kThreads)
 k_build_ends(const uint64_t *__restrict__ K, int64_t n, const uint32_t *__restrict__ node_start,
-             int64_t max_nodes, int4 *__restrict__ meta, DeviceParams *P)
+             int64_t max_nodes, int32_t leaf_cap, int4 *__restrict__ meta,
+             WalkNode *__restrict__ wnode, DeviceParams *P)
 {
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = node_start[n];
@@ -149,7 +157,15 @@ k_build_ends(const uint64_t *__restrict__ K, int64_t n, const uint32_t *__restri
         }
         end = lo;
     }
-    meta[k] = make_int4((int)node_start[end], (int)i, (int)(end - i), L);
+    int esc = (int)node_start[end];
+    if (!(esc > k && esc <= total)) {
+        atomicOr(&P->status, kStatusInternal);
+        esc = (int)total;
+    }
+    const int count = (int)(end - i);
+    const bool leaf = count <= leaf_cap || L == kLevels;
+    meta[k] = make_int4(esc, (int)i, count, L);
+    wnode[k].w = make_int4(esc, leaf ? esc : (int)k + 1, leaf ? count : 0, __float_as_int(P->s2[L]));
 }
 
 // A node whose mass is not finite or whose CoM lies at 2^126 or beyond is
@@ -171,15 +187,11 @@ __device__ __forceinline__ float4 store_moments(int64_t k, float sx, float sy, f
     return c;
 }
 
-// Stores a node's moments and its walk record {escape, the node a target
-// that does not accept it goes to next (escape for a leaf, which it opens;
-// k + 1 for an internal node, which it enters), leaf count (0 for an internal
-// node), bits of (side 2^-level)^2}.
-__device__ __forceinline__ void store_node(int64_t k, const int4 &m, bool leaf, float sx, float sy,
-                                           float sz, float M, float4 *sums,
-                                           WalkNode *wnode, DeviceParams *P)
+// Stores a node's moments: its sums, and {CoM, M} in its walk record (the
+// rest of the record comes from k_build_ends).
+__device__ __forceinline__ void store_node(int64_t k, float sx, float sy, float sz, float M,
+                                           float4 *sums, WalkNode *wnode, DeviceParams *P)
 {
-    wnode[k].w = make_int4(m.x, leaf ? m.x : (int)k + 1, leaf ? m.z : 0, __float_as_int(P->s2[m.w]));
     wnode[k].c = store_moments(k, sx, sy, sz, M, sums, P);
 }
 
@@ -213,7 +225,7 @@ k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ 
         sy = __fmaf_rn(p.w, p.y, sy);
         sz = __fmaf_rn(p.w, p.z, sz);
     }
-    store_node(k, m, true, sx, sy, sz, M, sums, wnode, P);
+    store_node(k, sx, sy, sz, M, sums, wnode, P);
     int64_t node = parent[k];
     while (node >= 0) {
         // release: this child's sums before the count; acquire: the last
@@ -240,7 +252,7 @@ k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ 
             }
             c = nc;
         }
-        store_node(node, meta[node], false, sx, sy, sz, M, sums, wnode, P);
+        store_node(node, sx, sy, sz, M, sums, wnode, P);
         node = parent[node];
     }
 }
@@ -261,7 +273,7 @@ void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &
         b.params);
     // the node count is only known on the device: cover the bound
     k_build_ends<<<ceil_div(b.max_nodes, kThreads), kThreads, 0, st>>>(
-        keys_sorted, b.n, b.node_start, b.max_nodes, b.meta, b.params);
+        keys_sorted, b.n, b.node_start, b.max_nodes, leaf_cap, b.meta, b.wnode, b.params);
     g_launches += 2;
 }
 

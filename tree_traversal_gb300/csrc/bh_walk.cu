@@ -30,9 +30,9 @@
 // needs no table lookup and no select on the leaf flag. An opened leaf's
 // particles are staged into shared memory once (one coalesced 16-byte load
 // per lane) and read back as broadcasts by every lane that opened it. The
-// loop is warp-uniform and bounded: k strictly increases, so a walk takes at
-// most num_nodes steps; the loop stops there and raises a status bit rather
-// than spin. The default width-64 kernel (k_walk_paired, below) holds two
+// loop is warp-uniform and ends within num_nodes steps without a per-step
+// bound: every record's next nodes lie in (k, num_nodes] (the build checks
+// each one), so the group's node index strictly increases. The default width-64 kernel (k_walk_paired, below) holds two
 // targets per lane and does their arithmetic in packed float2 instructions.
 //
 // The self term. When the target's own leaf is opened the oracle skips j = i.
@@ -217,7 +217,7 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
     uint32_t pc = 0, pp = 0;
     int steps = 0;
     int kb = __any_sync(gmask, valid) ? 0 : num_nodes;  // the ballot form's node
-    for (; steps <= num_nodes; ++steps) {
+    for (;; ++steps) {  // ends: the node index strictly increases
         const int k = kBallot ? kb : __reduce_min_sync(gmask, next);
         if (k >= num_nodes) break;
         const int4 w = kLocal ? loc.nodes[k].w : __ldg(&a.wnode[k].w);
@@ -376,7 +376,7 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
     uint32_t pc0 = 0, pc1 = 0, pp0 = 0, pp1 = 0;
     int next0 = v0 ? 0 : num_nodes, next1 = v1 ? 0 : num_nodes;
     int steps = 0;
-    for (; steps <= num_nodes; ++steps) {
+    for (;; ++steps) {  // ends: the node index strictly increases
         const int k = __reduce_min_sync(kFull, min(next0, next1));
         if (k >= num_nodes) break;
         const int4 w = kLocal ? loc.nodes[k].w : __ldg(&a.wnode[k].w);
@@ -540,7 +540,7 @@ __device__ __forceinline__ void together_walk(const WalkArgs &a, int num_nodes, 
     float ax = 0.0f, ay = 0.0f, az = 0.0f;
     uint32_t pc = 0, pp = 0;
     int k = 0, steps = 0;
-    for (; k < num_nodes && steps <= num_nodes; ++steps) {
+    for (; k < num_nodes; ++steps) {
         const int4 w = __ldg(&a.wnode[k].w);
         const float4 c = __ldg(&a.wnode[k].c);
         const float dx = __fsub_rn(c.x, xi.x);
@@ -611,7 +611,7 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
     float ax = 0.0f, ay = 0.0f, az = 0.0f;
     uint32_t pc = 0, pp = 0;
     int k = 0, steps = 0;
-    for (; steps <= num_nodes && k < num_nodes; ++steps) {
+    for (; k < num_nodes; ++steps) {
         const int4 w = __ldg(&a.wnode[k].w);
         const float4 c = __ldg(&a.wnode[k].c);
         const float dx = __fsub_rn(c.x, xi.x);
