@@ -150,7 +150,6 @@ size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
     b.sort_look = (uint32_t *)take(sizeof(uint32_t) * (size_t)sort_look_words(n));
     b.ps = (float4 *)take(sizeof(float4) * (size_t)n);
     b.lev_d = (int8_t *)take(n1);
-    b.lev_w = (int8_t *)take(n1);
     b.ncount = (uint8_t *)take(n1);
     b.pstart = (int32_t *)take(sizeof(int32_t) * n1);
     b.node_start = (uint32_t *)take(sizeof(uint32_t) * n1);

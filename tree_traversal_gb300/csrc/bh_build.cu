@@ -31,12 +31,12 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Per position: D (levels shared with the previous key), W (levels shared
-// with the key leaf_cap ahead), the number of nodes starting here, and the
-// start of the parent cell of the first of them.
+// Per position: D (levels shared with the previous key), the number of
+// nodes starting here (from D and W, the levels shared with the key leaf_cap
+// ahead), and the start of the parent cell of the first of them.
 __global__ void __launch_bounds__(kThreads)
 k_build_levels(const uint64_t *__restrict__ K, int64_t n, int32_t cap,
-               int8_t *__restrict__ lev_d, int8_t *__restrict__ lev_w,
+               int8_t *__restrict__ lev_d,
                uint8_t *__restrict__ ncount, int32_t *__restrict__ pstart)
 {
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -69,7 +69,6 @@ k_build_levels(const uint64_t *__restrict__ K, int64_t n, int32_t cap,
         if (Ws >= D) cnt = min(kLevels, max(D + 1, W + 1)) - D;  // parent over capacity
     }
     lev_d[i] = (int8_t)D;
-    lev_w[i] = (int8_t)W;
     ncount[i] = (uint8_t)cnt;
     pstart[i] = (int32_t)s;
 }
@@ -263,7 +262,7 @@ void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &
                   cudaStream_t st)
 {
     k_build_levels<<<ceil_div(b.n + 1, kThreads), kThreads, 0, st>>>(
-        keys_sorted, b.n, leaf_cap, b.lev_d, b.lev_w, b.ncount, b.pstart);
+        keys_sorted, b.n, leaf_cap, b.lev_d, b.ncount, b.pstart);
     g_launches += 1;
     // node_start = exclusive scan of ncount over n + 1 entries
     launch_scan_u8(b.ncount, b.node_start, b.n + 1, b.scan_partial, st);

@@ -62,7 +62,6 @@ struct Buffers {
     float4 *ps;               // sorted {x, y, z, m}
     // a5
     int8_t *lev_d;            // common levels with the previous key (-1 at 0)
-    int8_t *lev_w;            // common levels with the key leaf_cap ahead (-1 if none)
     uint8_t *ncount;          // nodes starting at each position
     int32_t *pstart;          // start of the parent cell of the first node at i
     uint32_t *node_start;     // [n + 1] exclusive scan of ncount
