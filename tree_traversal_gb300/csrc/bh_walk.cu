@@ -239,7 +239,7 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
             }
         }
         if (kBallot) kb = __any_sync(gmask, descend) ? k + 1 : w.x;
-        if (__any_sync(gmask, open)) {
+        if (w.z != 0 && __any_sync(gmask, open)) {  // w.z: group-uniform
             const int first = kLocal ? loc.first[k] : __ldg(&a.meta[k].y), count = w.z;
             if (first < 0 || first > a.n - count) {  // group-uniform consistency check
                 if (glane == 0) atomicOr(&a.P->status, kStatusInternal);
@@ -393,11 +393,13 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
             pc0 += acc0;
             pc1 += acc1;
         }
-        const bool leaf = w.z != 0;
-        const bool open0 = act0 && !acc0 && leaf, open1 = act1 && !acc1 && leaf;
+        // a target that neither accepts nor waits opens k if it is a leaf;
+        // the leaf test comes first: it is warp-uniform and skips the vote
+        // at internal nodes
+        const bool open0 = act0 && !acc0, open1 = act1 && !acc1;
         if (act0) next0 = acc0 ? w.x : w.y;
         if (act1) next1 = acc1 ? w.x : w.y;
-        if (__any_sync(kFull, open0 || open1)) {
+        if (w.z != 0 && __any_sync(kFull, open0 || open1)) {
             const int first = kLocal ? loc.first[k] : __ldg(&a.meta[k].y), count = w.z;
             if (first < 0 || first > a.n - count) {  // warp-uniform consistency check
                 if (lane == 0) atomicOr(&a.P->status, kStatusInternal);
