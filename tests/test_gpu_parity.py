@@ -90,10 +90,12 @@ CASES = {
     "unequal_masses_cap16": lambda: _masses(9000, 12),
     "uniform_20000_cap200": lambda: (*uniform_cube(20000, 6), 200),
     "two_spheres_2x8192": lambda: (*two_spheres(8192), 32),
-    # sizes on the radix tile and scan tile (2048 entries each) edges
+    # sizes on the scan tile (2048 entries) and radix tile (4096 keys; up to
+    # 4096 keys the sort is one block) edges
     "edge_2047": lambda: (*plummer(2047, 91), 32),
     "edge_4095": lambda: (*plummer(4095, 92), 32),
     "edge_8193_cap3": lambda: (*plummer(8193, 93), 3),
+    "edge_12287": lambda: (*plummer(12287, 94), 32),
 }
 _cache = {}
 
@@ -703,3 +705,34 @@ def test_fp32_fma_rate_is_within_the_pipes_nominal_range(tt):
     assert 0.5 < packed / scalar < 2.5
     # the rate per clock cannot exceed the 128 lanes of an SM
     assert 300 < r["sm_mhz"] < 2200 and scalar / (per_ghz * r["sm_mhz"] / 1000) <= 1.02, r
+
+
+
+# ---------------------------------------------------------------------------
+# the radix passes under skewed digits: every key equal (one digit per pass,
+# every tile's whole count in one bin), a few distinct points, keys sharing
+# their high digits, and sizes on the 4096-key tile edges; the tree (keys,
+# permutation, nodes, moments) bit-exact against the oracle
+# ---------------------------------------------------------------------------
+def _sort_stress(name):
+    rng = np.random.default_rng(5150)
+    if name == "all_equal_20000":
+        pos = np.full((20000, 3), 0.375, np.float32)
+    elif name == "seven_points_50000":
+        pts = rng.normal(size=(7, 3)).astype(np.float32)
+        pos = pts[rng.integers(0, 7, 50000)]
+    elif name == "tight_clump_40961":
+        pos = (1.0 + rng.normal(size=(40961, 3)) * 1e-5).astype(np.float32)
+        pos[:3] = [[-1.0, -1.0, -1.0], [2.0, 2.0, 2.0], [0.5, 0.5, 0.5]]  # a wide cube, a tiny clump
+    else:
+        n = int(name.split("_")[1])
+        pos, _ = plummer(n, 300 + n % 97)
+    return pos, np.full(len(pos), np.float32(1.0 / len(pos)), np.float32)
+
+
+@pytest.mark.parametrize("name", ["all_equal_20000", "seven_points_50000", "tight_clump_40961",
+                                  "plummer_8191", "plummer_8192", "plummer_12289", "plummer_16385"])
+def test_sort_stress_tree_bit_exact(tt, name):
+    pos, mass = _sort_stress(name)
+    T = oracle.Tree(pos, mass, 32)
+    check_tree(tt, pos, mass, 32, T)
