@@ -183,9 +183,14 @@ int orrery_bh_forces_range(const float *pos_d, const float *mass_d, int64_t n, f
 
 /*
  * The same evaluation from and to HOST memory (page-locked memory gives the
- * fastest copies; pageable memory works). The copies run on `stream` inside
- * the call; pos, mass and acc are required, interactions and visits may be
- * NULL. Shapes and order as in orrery_bh_forces.
+ * fastest copies; pageable memory works). The input copies run on `stream`
+ * inside the call; pos, mass and acc are required, interactions and visits
+ * may be NULL. Shapes and order as in orrery_bh_forces. An output buffer that
+ * is page-locked over its whole extent (cudaHostAlloc, cudaHostRegister) is
+ * written by the walk directly, over the host link while the walk runs; a
+ * pageable one is filled by a copy after the walk. Either way its contents
+ * are final when the call returns (the call blocks), and d2h_ms in the
+ * timings covers only the copies made.
  */
 int orrery_bh_forces_host(const float *pos, const float *mass, int64_t n, float theta, float eps,
                           int32_t leaf_cap, int32_t traversal, float *acc, uint32_t *interactions,

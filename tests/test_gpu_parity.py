@@ -257,6 +257,20 @@ def test_host_entry_point_matches_device(tt):
     assert np.array_equal(a2.view(np.uint32), acc.cpu().numpy().view(np.uint32))
 
 
+def test_host_entry_point_mixed_page_locked_and_pageable_outputs(tt):
+    """Page-locked outputs are written by the walk directly, pageable ones
+    copied after it: any mix gives the device entry point's bits."""
+    pos, mass, cap, T = case("plummer_131072")
+    acc, inter, vis = tt.bh_forces(dev(pos), dev(mass), 0.5, EPS, cap, "coherent64", fast_term=True)
+    big = torch.zeros(T.n * 3 + 64).pin_memory()  # a view inside a larger page-locked block
+    out = (big[64:].view(T.n, 3), np.zeros((T.n, 2), np.uint32),
+           torch.zeros(T.n, dtype=torch.int32).pin_memory())
+    tt.bh_forces_host(pos, mass, 0.5, EPS, cap, "coherent64", out=out, fast_term=True)
+    assert np.array_equal(out[0].numpy().view(np.uint32), acc.cpu().numpy().view(np.uint32))
+    assert np.array_equal(out[1], u32(inter)) and np.array_equal(out[2].numpy(), vis.cpu().numpy())
+    assert float(big[:64].abs().sum()) == 0.0  # nothing written outside the output
+
+
 def test_host_entry_point_without_counters(tt):
     pos, mass, cap, T = case("edge_4095")
     acc, _, _ = tt.bh_forces(dev(pos), dev(mass), 0.5, EPS, cap, "coherent64")

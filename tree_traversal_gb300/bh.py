@@ -108,7 +108,8 @@ def bh_forces_host(pos: np.ndarray, mass: np.ndarray, theta: float = 0.5, eps: f
                    leaf_cap: int = 32, traversal="coherent", out=None, device=None,
                    fast_term: bool = False):
     """The same evaluation from host arrays (numpy or CPU tensors, page-locked
-    for the fastest copies) to host arrays; the copies run inside the call.
+    for the fastest copies) to host arrays; the copies run inside the call,
+    and page-locked outputs are written by the walk directly.
     ``out`` = (acc [n,3] f32, interactions [n,2] u32 or None, visits [n] u32 or None);
     ``fast_term`` as for bh_forces."""
     def host_ptr(a, shape, dtype):
