@@ -159,7 +159,7 @@ size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
     b.nchild = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
     b.arrive = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
     b.sums = (float4 *)take(sizeof(float4) * (size_t)nodes);
-    b.wnode = (WalkNode *)take(sizeof(WalkNode) * (size_t)nodes);
+    b.wnode = (WalkNode *)take(sizeof(WalkNode) * ((size_t)nodes + 1));  // + the sentinel
     return off;
 }
 

@@ -135,6 +135,12 @@ k_build_ends(const uint64_t *__restrict__ K, int64_t n, const uint32_t *__restri
 {
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = node_start[n];
+    if (k == 0 && total <= max_nodes) {
+        // a sentinel after the last node: a leaf no target accepts (side^2 =
+        // +inf) with zero mass, where the packed walk's group ends
+        wnode[total].w = make_int4((int)total, (int)total, 1, 0x7f800000);
+        wnode[total].c = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
     if (k >= total || total > max_nodes) return;
     const int4 m = meta[k];
     const int64_t i = m.y;

@@ -72,7 +72,7 @@ struct Buffers {
     int32_t *arrive;          // [max_nodes]
     // a6
     float4 *sums;             // [max_nodes] {S_x, S_y, S_z, M}
-    WalkNode *wnode;          // [max_nodes] everything a walk step reads of a node
+    WalkNode *wnode;          // [max_nodes + 1] everything a walk step reads of a node, then a sentinel
 };
 
 // Kernel-launch counter (every launch site increments it).

@@ -80,7 +80,7 @@ size_t layout(Buffers &b, char *base, int64_t n, int64_t nodes)
     b.nchild = (int32_t *)take(4 * (size_t)nodes);
     b.arrive = (int32_t *)take(4 * (size_t)nodes);
     b.sums = (float4 *)take(16 * (size_t)nodes);
-    b.wnode = (WalkNode *)take(sizeof(WalkNode) * (size_t)nodes);
+    b.wnode = (WalkNode *)take(sizeof(WalkNode) * ((size_t)nodes + 1));  // + the sentinel
     return off;
 }
 

@@ -376,9 +376,11 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
     uint32_t pc0 = 0, pc1 = 0, pp0 = 0, pp1 = 0;
     int next0 = v0 ? 0 : num_nodes, next1 = v1 ? 0 : num_nodes;
     int steps = 0;
+    // k <= num_nodes: the record at num_nodes is a sentinel leaf that no
+    // target accepts (side^2 = +inf, zero mass), so when every target is done
+    // the group opens it, and the leaf branch ends the walk there
     for (;; ++steps) {  // ends: the node index strictly increases
         const int k = __reduce_min_sync(kFull, min(next0, next1));
-        if (k >= num_nodes) break;
         const int4 w = kLocal ? loc.nodes[k].w : __ldg(&a.wnode[k].w);
         const float4 c = kLocal ? loc.nodes[k].c : __ldg(&a.wnode[k].c);
         const bool act0 = next0 == k, act1 = next1 == k;
@@ -400,6 +402,7 @@ __device__ __forceinline__ void paired_walk(const WalkArgs &a, int num_nodes, fl
         if (act0) next0 = acc0 ? w.x : w.y;
         if (act1) next1 = acc1 ? w.x : w.y;
         if (w.z != 0 && __any_sync(kFull, open0 || open1)) {
+            if (k >= num_nodes) break;  // the sentinel
             const int first = kLocal ? loc.first[k] : __ldg(&a.meta[k].y), count = w.z;
             if (first < 0 || first > a.n - count) {  // warp-uniform consistency check
                 if (lane == 0) atomicOr(&a.P->status, kStatusInternal);
@@ -494,7 +497,8 @@ __global__ void __launch_bounds__(kBlock) k_walk_local(WalkArgs a)
     int num_nodes;
     bool self_free;
     if (!prologue<kFast>(a, num_nodes, self_free)) return;  // block-uniform
-    const int64_t tree_bytes = (int64_t)num_nodes * (sizeof(WalkNode) + sizeof(int));
+    // the node records with the sentinel, then the first indices
+    const int64_t tree_bytes = ((int64_t)num_nodes + 1) * sizeof(WalkNode) + (int64_t)num_nodes * sizeof(int);
     const int64_t ps_offset = (tree_bytes + 15) & ~int64_t(15);
     const bool with_ps = ps_offset + (int64_t)a.n * (int64_t)sizeof(float4) <= kLocalBytes;  // block-uniform
     // the group's slots of the per-warp leaf stage (a half warp at W = 16)
@@ -507,12 +511,12 @@ __global__ void __launch_bounds__(kBlock) k_walk_local(WalkArgs a)
         return;
     }
     WalkNode *nodes = reinterpret_cast<WalkNode *>(s_dyn);
-    int *first = reinterpret_cast<int *>(nodes + num_nodes);
+    int *first = reinterpret_cast<int *>(nodes + num_nodes + 1);
     float4 *ps = with_ps ? reinterpret_cast<float4 *>(s_dyn + ps_offset) : nullptr;
     {
         const int4 *src = reinterpret_cast<const int4 *>(a.wnode);
         int4 *dst = reinterpret_cast<int4 *>(nodes);
-        for (int i = threadIdx.x; i < 2 * num_nodes; i += kBlock) dst[i] = __ldg(src + i);
+        for (int i = threadIdx.x; i < 2 * (num_nodes + 1); i += kBlock) dst[i] = __ldg(src + i);
         for (int i = threadIdx.x; i < num_nodes; i += kBlock) first[i] = __ldg(&a.meta[i].y);
         if (with_ps)
             for (int i = threadIdx.x; i < a.n; i += kBlock) ps[i] = __ldg(a.ps + i);
