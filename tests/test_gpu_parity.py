@@ -725,16 +725,17 @@ def test_fp32_fma_rate_is_within_the_pipes_nominal_range(tt):
 # ---------------------------------------------------------------------------
 # the radix passes under skewed digits: every key equal (one digit per pass,
 # every tile's whole count in one bin), a few distinct points, keys sharing
-# their high digits, and sizes on the 4096-key tile edges; the tree (keys,
-# permutation, nodes, moments) bit-exact against the oracle
+# their high digits, sizes on the 4096-key tile edges, and both kinds of
+# tiles; the tree (keys, permutation, nodes, moments) bit-exact against the
+# oracle
 # ---------------------------------------------------------------------------
 def _sort_stress(name):
     rng = np.random.default_rng(5150)
-    if name == "all_equal_20000":
-        pos = np.full((20000, 3), 0.375, np.float32)
-    elif name == "seven_points_50000":
+    if name.startswith("all_equal_"):
+        pos = np.full((int(name.split("_")[2]), 3), 0.375, np.float32)
+    elif name.startswith("seven_points_"):
         pts = rng.normal(size=(7, 3)).astype(np.float32)
-        pos = pts[rng.integers(0, 7, 50000)]
+        pos = pts[rng.integers(0, 7, int(name.split("_")[2]))]
     elif name == "tight_clump_40961":
         pos = (1.0 + rng.normal(size=(40961, 3)) * 1e-5).astype(np.float32)
         pos[:3] = [[-1.0, -1.0, -1.0], [2.0, 2.0, 2.0], [0.5, 0.5, 0.5]]  # a wide cube, a tiny clump
@@ -745,7 +746,9 @@ def _sort_stress(name):
 
 
 @pytest.mark.parametrize("name", ["all_equal_20000", "seven_points_50000", "tight_clump_40961",
-                                  "plummer_8191", "plummer_8192", "plummer_12289", "plummer_16385"])
+                                  "plummer_8191", "plummer_8192", "plummer_12289", "plummer_16385",
+                                  # 8192-key tiles (above 622 592 keys)
+                                  "all_equal_700000", "seven_points_655361", "plummer_622593"])
 def test_sort_stress_tree_bit_exact(tt, name):
     pos, mass = _sort_stress(name)
     T = oracle.Tree(pos, mass, 32)

@@ -137,7 +137,6 @@ size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
     };
     b.n = n;
     b.max_nodes = nodes;
-    b.sort_tiles = sort_tiles_for(n);
     b.bbox_blocks = bbox_blocks_for(n);
     const size_t n1 = (size_t)n + 1;
     b.bbox_partial = (float *)take(sizeof(float) * 8 * (size_t)b.bbox_blocks);

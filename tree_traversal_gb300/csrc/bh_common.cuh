@@ -48,7 +48,6 @@ struct alignas(32) WalkNode {
 struct Buffers {
     int64_t n;
     int64_t max_nodes;
-    int sort_tiles;           // 4096-key tiles of the radix passes
     int bbox_blocks;
     // a1
     float *bbox_partial;      // [bbox_blocks][8]
@@ -57,7 +56,7 @@ struct Buffers {
     uint64_t *keys_a, *keys_b;
     uint32_t *idx_a, *idx_b;
     uint32_t *sort_ctl;       // [sort_ctl_words()] digit counts of every pass, tile tickets
-    uint32_t *sort_look;      // [2][sort_tiles][512] look-back words of alternate passes
+    uint32_t *sort_look;      // look-back words of alternate passes, [2][tiles][512]
     // a4
     float4 *ps;               // sorted {x, y, z, m}
     // a5
@@ -97,7 +96,6 @@ void launch_direct(const float *pos, const float *mass, int64_t n, float eps, fl
 void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *partial,
                     cudaStream_t st);
 int64_t scan_partial_count(int64_t count);
-int sort_tiles_for(int64_t n);
 int64_t sort_look_words(int64_t n);  // both look-back arrays
 int sort_ctl_words();
 void prepare_sort();  // sets the sort kernels' function attributes on this device

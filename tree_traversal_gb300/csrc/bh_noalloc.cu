@@ -58,7 +58,6 @@ size_t layout(Buffers &b, char *base, int64_t n, int64_t nodes)
     const size_t n1 = (size_t)n + 1;
     b.n = n;
     b.max_nodes = nodes;
-    b.sort_tiles = sort_tiles_for(n);
     int64_t bb = (n + 255) / 256;
     b.bbox_blocks = (int)(bb < 1 ? 1 : (bb > 1216 ? 1216 : bb));
     b.bbox_partial = (float *)take(sizeof(float) * 8 * (size_t)b.bbox_blocks);

@@ -12,16 +12,17 @@
 // 512-bin histograms), so every pass is a single launch in the manner of the
 // published "Onesweep" radix sort (Adinets and Merrill, 2022) with its
 // decoupled look-back (Merrill and Garland, 2016): a block takes the next
-// 4096-key tile by ticket, counts its digits, publishes the counts, and adds
-// up the counts of the tiles before it by reading their published words
-// backwards until it meets a tile that has already published its inclusive
-// prefix. A block only ever waits for tiles with smaller tickets, which are
-// already running, so every wait ends; each is still bounded, and a wait
-// that runs out flags an internal error instead of spinning on. The tile is
-// then ranked (each warp walks a contiguous 256-key span 32 keys at a time,
-// finding the lanes with equal digits by one vote per digit bit), put in
-// digit order in shared memory, and each digit's run is written to its
-// global slot with consecutive threads on consecutive addresses.
+// tile (4096 keys, or 8192 above 622 592 keys) by ticket, counts its
+// digits, publishes the counts, and adds up the counts of the tiles before
+// it by reading their published words backwards until it meets a tile that
+// has already published its inclusive prefix. A block only ever waits for
+// tiles with smaller tickets, which are already running, so every wait
+// ends; each is still bounded, and a wait that runs out flags an internal
+// error instead of spinning on. The tile is then ranked (each warp walks a
+// contiguous span of 256 or 512 keys, 32 keys at a time, finding the lanes
+// with equal digits by one vote per digit bit), put in digit order in shared
+// memory, and each digit's run is written to its global slot with
+// consecutive threads on consecutive addresses.
 #include <cuda/atomic>
 
 #include "bh_common.cuh"
@@ -31,13 +32,32 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 8;                       // per lane
-constexpr int kTile = kThreads * kItems;        // 4096 keys per block
-constexpr int kWarpSpan = 32 * kItems;          // 256 consecutive keys per warp
 constexpr int kBits = 9;
 constexpr int kBins = 1 << kBits;               // 512 digits
 constexpr int kPasses = 7;                      // 7 x 9 = 63 key bits
 constexpr int kBinsPerThread = kBins / kThreads;
+
+// One pass's tile: kItems keys per lane, so kThreads * kItems keys per block
+// and a contiguous span of 32 * kItems keys per warp. 4096-key tiles while
+// there are no more tiles than the 152 SMs, 8192-key tiles beyond (half the
+// tiles, so a shorter look-back chain and one block per SM where 4096-key
+// tiles would double up). Measured sort times: 0.080 vs 0.102 ms at 524 288
+// keys (128 tiles of 4096), 0.123 vs 0.107 ms at 786 432, 0.129 vs 0.111 ms
+// at 1M.
+template <int kItemsT>
+struct Tiling {
+    static constexpr int kItems = kItemsT;
+    static constexpr int kTile = kThreads * kItems;
+    static constexpr int kWarpSpan = 32 * kItems;
+    // a key's rank inside its warp's run of a digit is below the warp's
+    // span: one byte per key up to 256 keys per warp, else 16 bits
+    static constexpr int kRankBits = kWarpSpan <= 256 ? 8 : 16;
+    static constexpr int kRanksPerWord = 32 / kRankBits;
+    static constexpr uint32_t kRankMask = (1u << kRankBits) - 1u;
+};
+constexpr int kSmallTileItems = 8;   // 4096-key tiles
+constexpr int kLargeTileItems = 16;  // 8192-key tiles
+constexpr int64_t kLargeTileMinN = 152 * 4096 + 1;
 
 // Control words of one sort, cleared before the key kernel: the digit counts
 // of every pass, then one tile ticket per pass.
@@ -46,7 +66,7 @@ constexpr int kCtlWords = kCtlCounts + 8;
 
 // A look-back word: bit 31 set = the inclusive count of the digit over this
 // tile and all before it (at most 2^30, the largest n); bit 30 set = this
-// tile's own count only (at most 4096); zero = not yet published.
+// tile's own count only (at most 8192); zero = not yet published.
 constexpr uint32_t kLookInclusive = 0x80000000u;
 constexpr uint32_t kLookTileOnly = 0x40000000u;
 constexpr int kLookSpins = 1 << 20;  // polls of an unpublished word before giving up
@@ -183,14 +203,15 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *warp_sum, u
 
 
 // dynamic shared memory of one pass: digit counters and the reordered tile
+template <int kItems>
 struct PassSmem {
     uint32_t cnt[kWarps][kBins];  // per-warp digit counts, then offsets
     uint32_t base[kBins];         // global start of each digit's run for this tile
     uint32_t loc[kBins];          // start of each digit's run inside the tile
     uint32_t warp_sum[kWarps];
     uint32_t tile;                // this block's ticket = its tile
-    uint64_t key[kTile];
-    uint32_t val[kTile];
+    uint64_t key[Tiling<kItems>::kTile];
+    uint32_t val[Tiling<kItems>::kTile];
 };
 
 // Look-back words are read and written as device-scope relaxed atomics: each
@@ -209,6 +230,7 @@ __device__ __forceinline__ void look_store(uint32_t *p, uint32_t v)
 // totals; ticket: the pass's tile counter (zero on entry); look: the pass's
 // look-back words [tiles][kBins] (zero on entry); look_next: the next pass's
 // words, whose row for this tile is cleared here (null on the last pass).
+template <int kItems>
 __global__ void __launch_bounds__(kThreads)
 k_onesweep(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
            uint64_t *__restrict__ kout, uint32_t *__restrict__ vout, int64_t n, int pass,
@@ -216,7 +238,8 @@ k_onesweep(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
            uint32_t *look_next, int tiles, int *status)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    PassSmem &S = *reinterpret_cast<PassSmem *>(smem_raw);
+    using T = Tiling<kItems>;
+    PassSmem<kItems> &S = *reinterpret_cast<PassSmem<kItems> *>(smem_raw);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int shift = kBits * pass;
     if (threadIdx.x == 0) S.tile = atomicAdd(ticket, 1u);
@@ -247,16 +270,16 @@ k_onesweep(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
     }
     if (look_next)
         for (int d = threadIdx.x; d < kBins; d += kThreads) look_next[(int64_t)tile * kBins + d] = 0;
-    const int64_t tile0 = (int64_t)tile * kTile;
-    const int tile_n = (n - tile0 < (int64_t)kTile) ? (int)(n - tile0) : kTile;
+    const int64_t tile0 = (int64_t)tile * T::kTile;
+    const int tile_n = (n - tile0 < (int64_t)T::kTile) ? (int)(n - tile0) : T::kTile;
 
     // phase A: per-warp digit counts and each key's rank inside its warp's
-    // run of the digit (one byte per round: a warp holds 256 keys), spans
-    // walked in order
-    const int span = warp * kWarpSpan;
+    // run of the digit (packed kRanksPerWord to a register), spans walked in
+    // order
+    const int span = warp * T::kWarpSpan;
     uint64_t key[kItems];
     uint32_t val[kItems];
-    uint32_t rank[kItems / 4] = {};
+    uint32_t rank[(kItems + T::kRanksPerWord - 1) / T::kRanksPerWord] = {};
 #pragma unroll
     for (int r = 0; r < kItems; ++r) {
         const int e = span + r * 32 + lane;
@@ -267,7 +290,8 @@ k_onesweep(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
 #pragma unroll
     for (int r = 0; r < kItems; ++r) {
         const bool ok = span + r * 32 + lane < tile_n;
-        rank[r / 4] |= warp_rank(S.cnt[warp], digit_of(key[r], shift), ok) << (8 * (r % 4));
+        rank[r / T::kRanksPerWord] |= warp_rank(S.cnt[warp], digit_of(key[r], shift), ok)
+                                      << (T::kRankBits * (r % T::kRanksPerWord));
     }
     __syncthreads();
 
@@ -353,7 +377,9 @@ k_onesweep(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
     for (int r = 0; r < kItems; ++r) {
         if (span + r * 32 + lane < tile_n) {
             const uint32_t d = digit_of(key[r], shift);
-            const uint32_t p = S.loc[d] + S.cnt[warp][d] + ((rank[r / 4] >> (8 * (r % 4))) & 0xffu);
+            const uint32_t p = S.loc[d] + S.cnt[warp][d] +
+                               ((rank[r / T::kRanksPerWord] >> (T::kRankBits * (r % T::kRanksPerWord))) &
+                                T::kRankMask);
             if (p < (uint32_t)tile_n) {
                 S.key[p] = key[r];
                 S.val[p] = val[r];
@@ -510,12 +536,23 @@ void prepare_sort()
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !configured[dev].load()) {
-        cudaFuncSetAttribute(k_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(PassSmem));
+        cudaFuncSetAttribute(k_onesweep<kSmallTileItems>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(PassSmem<kSmallTileItems>));
+        cudaFuncSetAttribute(k_onesweep<kLargeTileItems>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(PassSmem<kLargeTileItems>));
         cudaFuncSetAttribute(k_radix_sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(SmallSortSmem));
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
+}
+
+static bool large_tiles(int64_t n) { return n >= kLargeTileMinN; }
+
+// Tiles of the passes for n keys (more than the single-block size).
+static int pass_tiles(int64_t n)
+{
+    const int tile = large_tiles(n) ? Tiling<kLargeTileItems>::kTile : Tiling<kSmallTileItems>::kTile;
+    return (int)((n + tile - 1) / tile);
 }
 
 // a2: the keys into b.keys_a; above the single-block size also the digit
@@ -532,7 +569,7 @@ void launch_morton(const float *pos, const Buffers &b, cudaStream_t st)
                      (kCountThreads * kCountKeysPerThread);
     if (blocks > kCountMaxBlocks) blocks = kCountMaxBlocks;
     k_keys_count<<<(unsigned)blocks, kCountThreads, 0, st>>>(
-        pos, b.n, b.params, b.keys_a, b.sort_ctl, b.sort_look, (int64_t)b.sort_tiles * kBins);
+        pos, b.n, b.params, b.keys_a, b.sort_ctl, b.sort_look, (int64_t)pass_tiles(b.n) * kBins);
     g_launches += 1;
 }
 
@@ -549,16 +586,21 @@ void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint
         *perm = b.idx_b;
         return;
     }
-    const int tiles = b.sort_tiles;
-    const int64_t look_words = (int64_t)tiles * kBins;
+    const int tiles = pass_tiles(b.n);
+    const int64_t look_words = (int64_t)tiles * kBins;  // the look-back rows of one pass
     uint64_t *kin = b.keys_a, *kout = b.keys_b;
     uint32_t *vin = b.idx_a, *vout = b.idx_b;
     for (int p = 0; p < kPasses; ++p) {
         uint32_t *look = b.sort_look + (p & 1) * look_words;
         uint32_t *look_next = p + 1 < kPasses ? b.sort_look + ((p + 1) & 1) * look_words : nullptr;
-        k_onesweep<<<tiles, kThreads, sizeof(PassSmem), st>>>(
-            kin, vin, kout, vout, b.n, p, b.sort_ctl + p * kBins, b.sort_ctl + kCtlCounts + p,
-            look, look_next, tiles, &b.params->status);
+        if (large_tiles(b.n))
+            k_onesweep<kLargeTileItems><<<tiles, kThreads, sizeof(PassSmem<kLargeTileItems>), st>>>(
+                kin, vin, kout, vout, b.n, p, b.sort_ctl + p * kBins, b.sort_ctl + kCtlCounts + p,
+                look, look_next, tiles, &b.params->status);
+        else
+            k_onesweep<kSmallTileItems><<<tiles, kThreads, sizeof(PassSmem<kSmallTileItems>), st>>>(
+                kin, vin, kout, vout, b.n, p, b.sort_ctl + p * kBins, b.sort_ctl + kCtlCounts + p,
+                look, look_next, tiles, &b.params->status);
         g_launches += 1;
         uint64_t *tk = kin;
         kin = kout;
@@ -571,9 +613,13 @@ void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint
     *perm = vin;
 }
 
-int sort_tiles_for(int64_t n) { return (int)((n + kTile - 1) / kTile); }
-
-int64_t sort_look_words(int64_t n) { return 2 * (int64_t)sort_tiles_for(n) * kBins; }
+// Both passes' look-back rows, sized for the smaller tiles whatever n (so
+// the size only grows with n, as the workspace assumes).
+int64_t sort_look_words(int64_t n)
+{
+    constexpr int tile = Tiling<kSmallTileItems>::kTile;
+    return 2 * ((n + tile - 1) / tile) * kBins;
+}
 
 int sort_ctl_words() { return kCtlWords; }
 
