@@ -32,8 +32,12 @@
 // per lane) and read back as broadcasts by every lane that opened it. The
 // loop is warp-uniform and ends within num_nodes steps without a per-step
 // bound: every record's next nodes lie in (k, num_nodes] (the build checks
-// each one), so the group's node index strictly increases. The default width-64 kernel (k_walk_paired, below) holds two
-// targets per lane and does their arithmetic in packed float2 instructions.
+// each one), so the group's node index strictly increases, and the record
+// at num_nodes is a sentinel leaf that no target accepts, so a group whose
+// targets are all done opens it and stops there, in the leaf branch, with no
+// per-step test of k. The default width-64 kernel (k_walk_paired, below)
+// holds two targets per lane and does their arithmetic in packed float2
+// instructions.
 //
 // The self term. When the target's own leaf is opened the oracle skips j = i.
 // Summing it instead changes nothing, bit for bit, whenever its force factor
@@ -217,9 +221,10 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
     uint32_t pc = 0, pp = 0;
     int steps = 0;
     int kb = __any_sync(gmask, valid) ? 0 : num_nodes;  // the ballot form's node
+    // k <= num_nodes: the group ends at the sentinel record after the last
+    // node (a leaf no target accepts), in the leaf branch, as the packed walk
     for (;; ++steps) {  // ends: the node index strictly increases
         const int k = kBallot ? kb : __reduce_min_sync(gmask, next);
-        if (k >= num_nodes) break;
         const int4 w = kLocal ? loc.nodes[k].w : __ldg(&a.wnode[k].w);
         const float4 c = kLocal ? loc.nodes[k].c : __ldg(&a.wnode[k].c);
         bool open = false, descend = false;
@@ -240,6 +245,7 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
         }
         if (kBallot) kb = __any_sync(gmask, descend) ? k + 1 : w.x;
         if (w.z != 0 && __any_sync(gmask, open)) {  // w.z: group-uniform
+            if (k >= num_nodes) break;  // the sentinel
             const int first = kLocal ? loc.first[k] : __ldg(&a.meta[k].y), count = w.z;
             if (first < 0 || first > a.n - count) {  // group-uniform consistency check
                 if (glane == 0) atomicOr(&a.P->status, kStatusInternal);
