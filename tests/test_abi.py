@@ -88,6 +88,10 @@ def test_argument_checks_answer_on_the_host(lib):
     assert d(dummy, dummy, 10, float("nan"), dummy, P) == L.EINVAL
     assert d(P, dummy, 10, 0.05, dummy, P) == L.EINVAL
     assert d(P, P, 0, 0.05, P, P) == L.OK
+    # the FMA-rate probe checks its outputs before touching the GPU
+    x = ctypes.c_double(0.0)
+    assert lib.orrery_fp32_fma_rate(None, ctypes.byref(x), None, None) == L.EINVAL
+    assert lib.orrery_fp32_fma_rate(ctypes.byref(x), None, None, None) == L.EINVAL
     # n == 0 launches nothing and succeeds, whatever the pointers
     assert f(P, P, 0, 0.5, 0.05, 32, 0, P, P, P, P) == L.OK
     assert lib.orrery_bh_forces_host(P, P, 0, 0.5, 0.05, 32, 1, P, P, P, P) == L.OK
