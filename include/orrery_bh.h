@@ -70,8 +70,12 @@ extern "C" {
 #define ORRERY_ENOMEM (-6)     /* the workspace could not be allocated (the environment
                                   variable ORRERY_FAIL_ALLOC=1 forces this whenever the
                                   workspace has to grow, to test callers' failure paths) */
-#define ORRERY_EINTERNAL (-7)  /* an index failed a device-side consistency check;
-                                  the access was skipped (a library defect) */
+#define ORRERY_EINTERNAL (-7)  /* an index failed a device-side consistency check,
+                                  or a bounded wait of the sort ran out; the access
+                                  or the wait was skipped (a library defect; the
+                                  environment variable ORRERY_TEST_SORT_STALL=1
+                                  forces the wait to run out, for failure-path
+                                  tests) */
 #define ORRERY_ESCRATCH (-8)   /* orrery_bh_forces_noalloc: the problem does not fit
                                   its fixed scratch array */
 

@@ -482,6 +482,21 @@ def test_allocation_failure_is_reported_and_recovered(tt, monkeypatch):
     assert bool(torch.isfinite(acc).all())
 
 
+def test_sort_wait_that_runs_out_is_reported_and_recovered(tt, monkeypatch):
+    """A tile that never publishes its digit counts (ORRERY_TEST_SORT_STALL=1
+    silences tile 0 of the first radix pass): the tiles after it give up their
+    bounded wait, the call reports ORRERY_EINTERNAL instead of hanging, and the
+    next call on the same inputs is exact again."""
+    pos, mass, cap, T = case("ragged_5003_cap7")  # two 4096-key tiles
+    p, m = dev(pos), dev(mass)
+    monkeypatch.setenv("ORRERY_TEST_SORT_STALL", "1")
+    with pytest.raises(tt.OrreryError) as e:
+        tt.bh_forces(p, m, 0.5, EPS, cap, "coherent64")
+    assert e.value.status == -7  # ORRERY_EINTERNAL
+    monkeypatch.delenv("ORRERY_TEST_SORT_STALL")
+    check_forces(tt, pos, mass, cap, T, 0.5, "coherent64")
+
+
 # ---------------------------------------------------------------------------
 # the opt-in fast term: same decisions and counts, accelerations within 1e-5
 # ---------------------------------------------------------------------------

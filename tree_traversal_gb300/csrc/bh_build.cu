@@ -37,8 +37,9 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads)
 k_build_levels(const uint64_t *__restrict__ K, int64_t n, int32_t cap,
                int8_t *__restrict__ lev_d,
-               uint8_t *__restrict__ ncount, int32_t *__restrict__ pstart)
+               uint8_t *__restrict__ ncount, int32_t *__restrict__ pstart, const int *status)
 {
+    if (*status & kStatusInternal) return;  // the keys are not sorted: build nothing
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i > n) return;
     if (i == n) {  // the scan runs over n + 1 entries; the last contributes 0
@@ -85,6 +86,7 @@ k_build_emit(int64_t n, const int8_t *__restrict__ lev_d, const uint8_t *__restr
              int64_t max_nodes, int4 *__restrict__ meta, int32_t *__restrict__ parent,
              int32_t *__restrict__ nchild, DeviceParams *P)
 {
+    if (P->status & kStatusInternal) return;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const uint32_t total = node_start[n];
@@ -133,6 +135,7 @@ k_build_ends(const uint64_t *__restrict__ K, int64_t n, const uint32_t *__restri
              int64_t max_nodes, int32_t leaf_cap, int4 *__restrict__ meta,
              WalkNode *__restrict__ wnode, DeviceParams *P)
 {
+    if (P->status & kStatusInternal) return;
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = node_start[n];
     if (k == 0 && total <= max_nodes) {
@@ -214,7 +217,7 @@ k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ 
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const int cnt = ncount[i];
-    if (cnt == 0 || (P->status & kStatusNodeBound)) return;
+    if (cnt == 0 || (P->status & (kStatusNodeBound | kStatusInternal))) return;
     int64_t k = (int64_t)node_start[i] + cnt - 1;
     const int4 m = meta[k];
     if (m.y < 0 || m.z < 0 || (int64_t)m.y + m.z > n) {
@@ -268,7 +271,7 @@ void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &
                   cudaStream_t st)
 {
     k_build_levels<<<ceil_div(b.n + 1, kThreads), kThreads, 0, st>>>(
-        keys_sorted, b.n, leaf_cap, b.lev_d, b.ncount, b.pstart);
+        keys_sorted, b.n, leaf_cap, b.lev_d, b.ncount, b.pstart, &b.params->status);
     g_launches += 1;
     // node_start = exclusive scan of ncount over n + 1 entries
     launch_scan_u8(b.ncount, b.node_start, b.n + 1, b.scan_partial, st);

@@ -144,7 +144,7 @@ k_gather(const float *__restrict__ pos, const float *__restrict__ mass,
          const uint32_t *__restrict__ perm, int64_t n, float4 *__restrict__ ps, int *status)
 {
     int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= n) return;
+    if (k >= n || (*status & kStatusInternal)) return;  // no permutation to follow
     uint32_t i = __ldg(perm + k);
     if (i >= (uint64_t)n) {
         atomicOr(status, kStatusInternal);

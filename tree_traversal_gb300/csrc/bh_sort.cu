@@ -23,6 +23,8 @@
 // with equal digits by one vote per digit bit), put in digit order in shared
 // memory, and each digit's run is written to its global slot with
 // consecutive threads on consecutive addresses.
+#include <stdlib.h>
+
 #include <cuda/atomic>
 
 #include "bh_common.cuh"
@@ -70,6 +72,10 @@ constexpr int kCtlWords = kCtlCounts + 8;
 constexpr uint32_t kLookInclusive = 0x80000000u;
 constexpr uint32_t kLookTileOnly = 0x40000000u;
 constexpr int kLookSpins = 1 << 20;  // polls of an unpublished word before giving up
+// ORRERY_TEST_SORT_STALL=1 (failure-path tests): tile 0 of the first pass
+// never publishes its counts, and the tiles after it give up after this many
+// polls, flag an internal error and go on
+constexpr int kTestLookSpins = 64;
 constexpr int kLookWindow = 4;       // earlier tiles' words read at once
 
 // Spreads the low 21 bits of v so that bit b lands at bit 3b.
@@ -229,13 +235,15 @@ __device__ __forceinline__ void look_store(uint32_t *p, uint32_t v)
 // One pass over the tile of this block's ticket. counts: the pass's digit
 // totals; ticket: the pass's tile counter (zero on entry); look: the pass's
 // look-back words [tiles][kBins] (zero on entry); look_next: the next pass's
-// words, whose row for this tile is cleared here (null on the last pass).
+// words, whose row for this tile is cleared here (null on the last pass);
+// silent_tile: a tile that publishes nothing (-1: none; failure-path tests
+// only); spin_limit: polls of an unpublished word before giving up.
 template <int kItems>
 __global__ void __launch_bounds__(kThreads)
 k_onesweep(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
            uint64_t *__restrict__ kout, uint32_t *__restrict__ vout, int64_t n, int pass,
            const uint32_t *__restrict__ counts, uint32_t *ticket, uint32_t *look,
-           uint32_t *look_next, int tiles, int *status)
+           uint32_t *look_next, int tiles, int silent_tile, int spin_limit, int *status)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     using T = Tiling<kItems>;
@@ -309,7 +317,7 @@ k_onesweep(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
             run += x;
         }
         c[q] = run;
-        look_store(row + d, (tile == 0 ? kLookInclusive : kLookTileOnly) | run);
+        if (tile != silent_tile) look_store(row + d, (tile == 0 ? kLookInclusive : kLookTileOnly) | run);
     }
 
     // look-back: the count of each digit over all earlier tiles, reading the
@@ -344,7 +352,7 @@ k_onesweep(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
                 if (found) break;
                 j -= used;
                 if (used == 0) {  // tile j has not published yet
-                    if (++spins > kLookSpins) {  // it never did: give up, flagged
+                    if (++spins > spin_limit) {  // it never did: give up, flagged
                         atomicOr(status, kStatusInternal);
                         break;
                     }
@@ -352,7 +360,7 @@ k_onesweep(const uint64_t *__restrict__ kin, const uint32_t *__restrict__ vin,
                     pause = pause < 1024 ? 2 * pause : pause;
                 }
             }
-            look_store(row + d, kLookInclusive | (before + c[q]));
+            if (tile != silent_tile) look_store(row + d, kLookInclusive | (before + c[q]));
         }
         S.base[d] = start[q] + before;
     }
@@ -588,6 +596,8 @@ void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint
     }
     const int tiles = pass_tiles(b.n);
     const int64_t look_words = (int64_t)tiles * kBins;  // the look-back rows of one pass
+    const char *stall = getenv("ORRERY_TEST_SORT_STALL");
+    const bool stalled = stall && stall[0] == '1';
     uint64_t *kin = b.keys_a, *kout = b.keys_b;
     uint32_t *vin = b.idx_a, *vout = b.idx_b;
     for (int p = 0; p < kPasses; ++p) {
@@ -596,11 +606,13 @@ void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint
         if (large_tiles(b.n))
             k_onesweep<kLargeTileItems><<<tiles, kThreads, sizeof(PassSmem<kLargeTileItems>), st>>>(
                 kin, vin, kout, vout, b.n, p, b.sort_ctl + p * kBins, b.sort_ctl + kCtlCounts + p,
-                look, look_next, tiles, &b.params->status);
+                look, look_next, tiles, stalled && p == 0 ? 0 : -1,
+                stalled ? kTestLookSpins : kLookSpins, &b.params->status);
         else
             k_onesweep<kSmallTileItems><<<tiles, kThreads, sizeof(PassSmem<kSmallTileItems>), st>>>(
                 kin, vin, kout, vout, b.n, p, b.sort_ctl + p * kBins, b.sort_ctl + kCtlCounts + p,
-                look, look_next, tiles, &b.params->status);
+                look, look_next, tiles, stalled && p == 0 ? 0 : -1,
+                stalled ? kTestLookSpins : kLookSpins, &b.params->status);
         g_launches += 1;
         uint64_t *tk = kin;
         kin = kout;
