@@ -344,13 +344,15 @@ def run_reference(args, rank: int, world: int) -> None:
     pos, mass, params = workload(args.workload)
     if args.theta is not None:
         params["theta"] = args.theta
-    times, vals = [], []
+    times, vals, walk1, walk_all = [], [], [], []
     cb = None
     for step in range(args.warmup + args.steps):
         cb = cpu_baseline(pos, mass, params, min(args.cpu_seconds, 4.0))
         if step >= args.warmup:
             times.append(cb["ms_per_evaluation_est"])
             vals.append(cb["value"])
+            walk1.append(cb["walk_interactions_per_s_1_thread"])
+            walk_all.append(cb["walk_interactions_per_s_all_threads"])
     v = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
@@ -359,7 +361,9 @@ def run_reference(args, rank: int, world: int) -> None:
             "config": {"workload": args.workload, "n": int(pos.shape[0]), **params,
                        "traversal": "independent (CPU oracle)"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
-                             "sample": cb["sample"]},
+                             "sample": cb["sample"],
+                             "walk_interactions_per_s_1_thread": statistics.median(walk1),
+                             "walk_interactions_per_s_all_threads": statistics.median(walk_all)},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
