@@ -158,7 +158,7 @@ k_morton(const float *__restrict__ pos, int64_t n, const DeviceParams *__restric
 // in shared memory and adds its histograms to the global ones; the grid also
 // clears the look-back words of the first pass.
 constexpr int kCountThreads = 512;
-constexpr int kCountKeysPerThread = 16;
+constexpr int kCountKeysPerThread = 4;   // more blocks, more keys in flight
 constexpr int kCountMaxBlocks = 2 * 152;
 
 __global__ void __launch_bounds__(kCountThreads)
