@@ -1,0 +1,28 @@
+"""bench.py's host-side bookkeeping, on the CPU: the walk's DRAM traffic is
+taken from the committed ncu summary only while the profiled kernel source
+is the current one."""
+from __future__ import annotations
+
+import os
+import shutil
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+WALK_SRC = os.path.join(ROOT, "tree_traversal_gb300", "csrc", "bh_walk.cu")
+
+
+def test_committed_traffic_matches_the_current_walk_source():
+    # the summary the default bench line reads was captured on this source
+    traffic = bench.profile_traffic(WALK_SRC, "k_walk_paired", True)
+    assert traffic is not None and 40e6 < traffic < 120e6
+
+
+def test_traffic_is_withheld_for_a_changed_source(tmp_path):
+    changed = tmp_path / "bh_walk.cu"
+    shutil.copy(WALK_SRC, changed)
+    with open(changed, "a") as f:
+        f.write("\n// changed\n")
+    assert bench.profile_traffic(str(changed), "k_walk_paired", True) is None
+    # and for a walk kernel with no summary of its own
+    assert bench.profile_traffic(WALK_SRC, "k_walk_independent", True) is None
