@@ -257,13 +257,18 @@ def test_cube_is_numpy_min_max():
     assert np.all(oracle.keys(np.ones((5, 3), np.float32)) == 0)
 
 
-def test_sort_is_stable_argsort():
+def pin_sort_stable():
+    # many equal keys: the order among them is the original index order
     rng = np.random.default_rng(5)
     keys = rng.integers(0, 50, 5000).astype(np.uint64) << np.uint64(40)
     perm, sk = oracle.sort(keys)
     ref = np.argsort(keys, kind="stable")
     assert np.array_equal(perm, ref.astype(np.uint32))
     assert np.array_equal(sk, keys[ref])
+
+
+def test_sort_is_stable_argsort():
+    pin_sort_stable()
 
 
 # ---------------------------------------------------------------------------
@@ -647,6 +652,10 @@ MISTAKES = [
      "return 1.0f / sqrtf(x);\n    float y = 0; const double xd = (double)x;", pin_rsqrt_rn),
     ("cell term uses the target's mass", "add_term(xi, c[0], c[1], c[2], c[3], eps2, acc);",
      "add_term(xi, c[0], c[1], c[2], t->ps[4 * i + 3], eps2, acc);", pin_far_clump),
+    ("equal keys in descending index order", "if (a->index != b->index) return (a->index < b->index) ? -1 : 1;",
+     "if (a->index != b->index) return (a->index > b->index) ? -1 : 1;", pin_sort_stable),
+    ("keys sorted descending", "if (a->key != b->key) return (a->key < b->key) ? -1 : 1;",
+     "if (a->key != b->key) return (a->key > b->key) ? -1 : 1;", pin_sort_stable),
 ]
 
 
