@@ -244,7 +244,7 @@ def test_quantise_floor_and_clamp():
         assert oracle.quantise(np.nextafter(np.float32(x), np.float32(0)), 0.0, inv) == j - 1
 
 
-def test_cube_is_numpy_min_max():
+def pin_cube():
     for n, seed in ((1, 1), (2, 2), (1000, 3)):
         pos, _ = uniform_cube(n, seed, -3.0, 5.0)
         lo, side, inv = oracle.cube(pos)
@@ -252,9 +252,19 @@ def test_cube_is_numpy_min_max():
         assert side == np.float32((pos.max(0) - pos.min(0)).max())
         if side > 0:
             assert inv == np.float32(2 ** 21) / side
+    # the largest extent on each axis in turn: the side is the largest of the three
+    for axis in range(3):
+        pos, _ = uniform_cube(200, 10 + axis, -1.0, 1.0)
+        pos[:, axis] *= 4.0
+        lo, side, inv = oracle.cube(pos)
+        assert side == np.float32((pos.max(0) - pos.min(0)).max())
     lo, side, inv = oracle.cube(np.ones((5, 3), np.float32))
     assert side == 0 and inv == 0
     assert np.all(oracle.keys(np.ones((5, 3), np.float32)) == 0)
+
+
+def test_cube_is_numpy_min_max():
+    pin_cube()
 
 
 def pin_sort_stable():
@@ -656,6 +666,9 @@ MISTAKES = [
      "if (a->index != b->index) return (a->index > b->index) ? -1 : 1;", pin_sort_stable),
     ("keys sorted descending", "if (a->key != b->key) return (a->key < b->key) ? -1 : 1;",
      "if (a->key != b->key) return (a->key > b->key) ? -1 : 1;", pin_sort_stable),
+    ("a cell of exactly leaf_cap particles split", "int is_leaf = (count <= st->leaf_cap) || (level == ORACLE_LEVELS);",
+     "int is_leaf = (count < st->leaf_cap) || (level == ORACLE_LEVELS);", pin_tree_brute_force),
+    ("cube side from the first axis alone", "if (ext > s) s = ext;", "if (a == 0) s = ext;", pin_cube),
 ]
 
 
