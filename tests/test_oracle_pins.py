@@ -234,7 +234,7 @@ def test_rsqrt_newton_within_two_ulp():
     pin_rsqrt_newton()
 
 
-def test_quantise_floor_and_clamp():
+def pin_quantise():
     inv = np.float32(2 ** 21)  # side 1
     assert oracle.quantise(0.0, 0.0, inv) == 0
     assert oracle.quantise(1.0, 0.0, inv) == 2 ** 21 - 1  # clamped
@@ -242,6 +242,10 @@ def test_quantise_floor_and_clamp():
         x = j / 2 ** 21  # exact binary fractions: the product is exact
         assert oracle.quantise(x, 0.0, inv) == j
         assert oracle.quantise(np.nextafter(np.float32(x), np.float32(0)), 0.0, inv) == j - 1
+
+
+def test_quantise_floor_and_clamp():
+    pin_quantise()
 
 
 def pin_cube():
@@ -669,6 +673,10 @@ MISTAKES = [
     ("a cell of exactly leaf_cap particles split", "int is_leaf = (count <= st->leaf_cap) || (level == ORACLE_LEVELS);",
      "int is_leaf = (count < st->leaf_cap) || (level == ORACLE_LEVELS);", pin_tree_brute_force),
     ("cube side from the first axis alone", "if (ext > s) s = ext;", "if (a == 0) s = ext;", pin_cube),
+    ("quantise rounds instead of flooring", "return (uint32_t)floorf(t);", "return (uint32_t)roundf(t);",
+     pin_quantise),
+    ("no clamp at the top of the cube", "if (t >= 2097151.0f) return 2097151u;",
+     "if (t >= 2097152.0f) return 2097152u;", pin_golden_three_points),
 ]
 
 
