@@ -677,6 +677,14 @@ MISTAKES = [
      pin_quantise),
     ("no clamp at the top of the cube", "if (t >= 2097151.0f) return 2097151u;",
      "if (t >= 2097152.0f) return 2097152u;", pin_golden_three_points),
+    ("an internal node's first child left out of its sums", "int64_t c = k + 1;\n        while (c < node[0]) {",
+     "int64_t c = nodes[4 * (k + 1) + 0];\n        while (c < node[0]) {", pin_moments),
+    ("the x sum used for the y coordinate of the CoM", "cm[4 * k + 1] = (M > 0.0f) ? sy / M : 0.0f;",
+     "cm[4 * k + 1] = (M > 0.0f) ? sx / M : 0.0f;", pin_moments),
+    ("an opened leaf's last particle left out",
+     "for (int64_t j = node[1]; j < (int64_t)node[1] + node[2]; ++j) {\n                if (j == i) continue;",
+     "for (int64_t j = node[1]; j < (int64_t)node[1] + node[2] - 1; ++j) {\n                if (j == i) continue;",
+     pin_theta0_is_direct),
 ]
 
 
