@@ -118,7 +118,8 @@ typedef enum {
 typedef struct {
     float h2d_ms;     /* orrery_bh_forces_host only: host-to-device copies */
     float bbox_ms;    /* bounding cube reduction */
-    float morton_ms;  /* quantise + interleave */
+    float morton_ms;  /* quantise + interleave (above 4096 particles also the
+                         digit counts of every radix pass) */
     float sort_ms;    /* radix sort of (key, index) */
     float gather_ms;  /* particles into tree order */
     float build_ms;   /* octree nodes and escape indices */
