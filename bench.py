@@ -4,9 +4,13 @@ A step is one whole evaluation through the C ABI (bounding cube, Morton keys,
 radix sort, gather, octree build, moments, coherent walk, scatter) with the
 inputs already resident in device memory. Prints one JSON line.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--theta T]
                     [--traversal coherent64|coherent|independent|...] [--term fast|exact]
-                    [--impl ours|reference]
+                    [--impl ours|reference] [--scaling | --crossover]
+
+--scaling runs the evaluation from 1 024 to 16 777 216 particles (one JSON
+line per size); --crossover times the tree against direct summation from
+1 024 to 262 144 particles.
 
 --impl reference times the CPU oracle (the plain C restatement of the
 method) on this host's cores instead, on a bounded sample of the same
