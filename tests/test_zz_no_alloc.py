@@ -82,6 +82,20 @@ def test_noalloc_every_traversal(lib):
             assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
+def test_noalloc_documented_sizes_fit(lib):
+    """The header's promise: every n up to 65 536 fits at leaf_cap 16 and up to
+    80 000 at leaf_cap 32 (the layout's limits are 75 827 and 95 488)."""
+    import tree_traversal_gb300._lib as L
+    from inputs import plummer
+
+    for n, cap in ((65536, 16), (80000, 32)):
+        pos, mass = plummer(n, 41)
+        p, m = torch.from_numpy(pos).cuda(), torch.from_numpy(mass).cuda()
+        rc, acc, inter, vis = _call(lib.orrery_bh_forces_noalloc, p, m, 0.5, 0.05, cap, L.COHERENT)
+        assert rc == L.OK, (n, cap, rc)
+        assert bool(torch.isfinite(acc).all())
+
+
 def test_noalloc_rejects_what_does_not_fit(lib):
     import tree_traversal_gb300._lib as L
 
