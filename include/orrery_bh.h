@@ -27,15 +27,26 @@
  *              nodes sum their children in order; CoM = S / M (0 if M <= 0)
  *   criterion: accept iff (side 2^-L)^2 < (theta^2) * d2, d2 = |CoM - x_i|^2
  *              formed as fma(dz, dz, fma(dy, dy, dx * dx))
- *   term:      r2 = d2 + eps^2 (d2 of the source, cell CoM or particle);
- *              y = 1/sqrt(r2) by a fixed recipe: the bit-level seed
- *              0x5f375a86 - bits(r2)/2 (C. Lomont, 2003) and three
- *              Newton-Raphson steps y (3/2 - (r2/2) y^2), within 2 ulp;
- *              f = (m y)(y y); a_i += f (x_src - x_i) by fused multiply-add,
- *              in walk order. With ORRERY_FAST_TERM y is the hardware
- *              approximation instead.
- * Every traversal except the descend-together contrast gives bit-identical
- * accelerations and interaction counts.
+ *   term:      the workloads' softened law a_i += m (x_src - x_i) /
+ *              (r^2 + eps^2)^(3/2), G = 1, over the target's own accepted
+ *              cells (M, CoM) and opened leaves' particles j != i, in
+ *              single precision. The kernels form r2 = d2 + eps^2 and
+ *              y = 1/sqrt(r2) by a fixed recipe (the bit-level seed
+ *              0x5f375a86 - bits(r2)/2 of C. Lomont, 2003, and three
+ *              Newton-Raphson steps, within 2 ulp) or, with
+ *              ORRERY_FAST_TERM, by the hardware approximation; then
+ *              f = (m y)(y y) and a_i += f (x_src - x_i) by fused
+ *              multiply-add. Each target's summation order depends only on
+ *              the tree. Against the law evaluated plainly in binary32
+ *              (m / (r2 sqrt(r2))) every target is within 1e-5 relative
+ *              error on softened Plummer inputs (measured at most a few
+ *              1e-6); where a target's terms nearly cancel the deviation is
+ *              a few 1e-7 of the summed magnitude of its terms instead.
+ * The acceptance tests, and so the interaction and visit counts, do not
+ * depend on the term: they are exact, equal to a CPU restatement of the
+ * steps above bit for bit. Every traversal except the descend-together
+ * contrast gives the same counts; the independent and the coherent walks of
+ * width 16, 32 and 64 also the same accelerations, bit for bit.
  *
  * Memory: every pointer named *_d or documented "device" is a CUDA device
  * pointer on the current device, owned by the caller. The library owns a
@@ -79,8 +90,9 @@ extern "C" {
 #define ORRERY_ESCRATCH (-8)   /* orrery_bh_forces_noalloc: the problem does not fit
                                   its fixed scratch array */
 
-/* Which traversal the walk kernel runs ("sycl_tree_solver.hpp",
- * TreeTraversal). Values 0-3 and 5 compute the same function of the input; the
+/* Which traversal the walk kernel runs ("sycl_tree_solver.hpp", enum
+ * TreeTraversal {kIndependent, kCoherent}; the coherent walk as ADR-0029,
+ * Decision, defines it). Values 0-3 and 5 compute the same function of the input; the
  * coherent ones differ only in how many consecutive sorted targets share one
  * node index (the coherence width; docs/performance/sycl_tree.md, "The
  * sub-group width"), which changes the visit counts they report and their
@@ -102,15 +114,11 @@ typedef enum {
 /* Flag ORed into the traversal argument: the force term's inverse square
  * root uses the hardware approximation (rsqrt.approx) instead of the fixed
  * Newton sequence. The width-64 walk is then ~20 % faster; acceptance
- * decisions, counts and visits are unchanged, and accelerations agree with
- * the exact path to rounding instead of bit for bit: at most 4.4e-6 relative
- * on the Plummer and two-sphere workloads (softening 0.05, 1M-2M particles),
- * bounded by 1e-5 in the tests at softening 0.05 and above. In general the
- * deviation of a target is a few 1e-7 of the summed magnitude of its terms,
- * so a target whose terms nearly cancel shows a larger relative deviation
- * (1.6e-5 seen without softening, 2.6e-5 at the centre of a uniform cube
- * with theta 1.2): where that matters the exact term is the one to use.
- * Without the flag results are reproducible bit for bit on any IEEE-754 CPU. */
+ * decisions, counts and visits are unchanged, and accelerations stay within
+ * the same bounds against the plainly evaluated law (see the file head).
+ * Without the flag the term is a fixed sequence of IEEE-754 binary32
+ * operations, so the accelerations are reproducible bit for bit on any
+ * IEEE-754 CPU that repeats them. */
 #define ORRERY_FAST_TERM 0x100
 
 /* Where the last evaluation spent its time ("sycl_tree_solver.hpp",
@@ -137,7 +145,10 @@ typedef struct {
 } orrery_bh_timings;
 
 /*
- * Evaluates accelerations for n particles.
+ * Evaluates accelerations for n particles: one force evaluation of the pages'
+ * solver ("sycl_tree_solver.hpp", Detailed Description: the particles are
+ * gathered into tree order, every target walks the octree, the results are
+ * scattered back to the caller's order), with every phase on the device.
  *   pos_d        device, float32 [n][3] contiguous (x, y, z per particle)
  *   mass_d       device, float32 [n]
  *   n            0 <= n <= 2^30; n == 0 returns ORRERY_OK and launches nothing
@@ -216,12 +227,21 @@ int orrery_bh_forces_host(const float *pos, const float *mass, int64_t n, float 
  * every n <= 80000 fits. A call that does not fit returns ORRERY_ESCRATCH
  * before launching anything.
  *
- * The first call on each device looks up the array's device address (with
- * that device current) and caches it: make that first call before any stream
- * capture. All calls share the array, which keeps the previous call's
- * contents; each call clears what must start at zero. Calls whose GPU work
- * overlapped would race on the array: this entry point serialises its calls
- * and waits for its own work before returning, so its calls do not overlap.
+ * Every call looks up the array's device address on the caller's current
+ * device (so a context torn down by cudaDeviceReset and created again is
+ * handled). The first call on a device may load the library's device code
+ * there and sets kernel attributes: make it before any stream capture. All
+ * calls share the array, which keeps the previous call's contents; each call
+ * clears what must start at zero. Calls whose GPU work overlapped would race
+ * on the array: this entry point serialises its calls and waits for its own
+ * work before returning, so its calls do not overlap.
+ *
+ * Each call ends by copying a status word to the host and synchronising
+ * `stream`. If another thread may be capturing a CUDA graph meanwhile, pass a
+ * stream created with cudaStreamNonBlocking (not the legacy NULL stream),
+ * and have the capturing thread use cudaStreamCaptureModeThreadLocal or
+ * cudaStreamCaptureModeRelaxed: under the global mode a synchronising call
+ * from another thread invalidates that capture.
  * Arguments, layouts, results and statuses as in orrery_bh_forces; no phase
  * timings are recorded.
  */

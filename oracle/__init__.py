@@ -101,10 +101,6 @@ def _bind(lib):
     lib.oracle_cube.restype = None
     lib.oracle_quantise.argtypes = [f32, f32, f32]
     lib.oracle_quantise.restype = ctypes.c_uint32
-    lib.oracle_rsqrt_rn.argtypes = [f32]
-    lib.oracle_rsqrt_rn.restype = f32
-    lib.oracle_rsqrt_newton.argtypes = [f32]
-    lib.oracle_rsqrt_newton.restype = f32
     lib.oracle_interleave.argtypes = [ctypes.c_uint32] * 3
     lib.oracle_interleave.restype = ctypes.c_uint64
     lib.oracle_keys.argtypes = [P, i64, P, f32, P]
@@ -130,6 +126,8 @@ def _bind(lib):
     lib.oracle_bh_forces.restype = i64
     lib.oracle_direct_f64.argtypes = [P, P, i64, f64, P, i64, P, ctypes.c_int]
     lib.oracle_direct_f64.restype = ctypes.c_int
+    lib.oracle_term_magnitude_f64.argtypes = [P, P, i64, f64, P, i64, P, ctypes.c_int]
+    lib.oracle_term_magnitude_f64.restype = ctypes.c_int
     lib.oracle_direct_f32.argtypes = [P, P, i64, f32, P, i64, P, ctypes.c_int]
     lib.oracle_direct_f32.restype = ctypes.c_int
     lib.oracle_bh_recursive.argtypes = [P, P, i64, i32, f32, f32, f32, P, P]
@@ -170,16 +168,6 @@ def cube(pos) -> tuple[np.ndarray, np.float32, np.float32]:
 # --------------------------------------------------------------------------
 def quantise(x: float, lo: float, inv: float) -> int:
     return int(_load().oracle_quantise(float(x), float(lo), float(inv)))
-
-
-def rsqrt_rn(x: float) -> np.float32:
-    """The binary32 value nearest 1/sqrt(x) (the force term's inverse root)."""
-    return np.float32(_load().oracle_rsqrt_rn(float(np.float32(x))))
-
-
-def rsqrt_newton(x: float) -> np.float32:
-    """The force term's inverse square root (fixed seed + three Newton steps)."""
-    return np.float32(_load().oracle_rsqrt_newton(float(np.float32(x))))
 
 
 def interleave(qx: int, qy: int, qz: int) -> int:
@@ -388,6 +376,26 @@ def direct_f32(pos, mass, eps: float = 0.05, targets=None, threads: int | None =
                                    _ptr(out), int(threads or default_threads()))
     if rc != 0:
         raise RuntimeError("oracle_direct_f32")
+    return out
+
+
+def term_magnitude_f64(pos, mass, eps: float = 0.05, targets=None,
+                       threads: int | None = None) -> np.ndarray:
+    """Per target, the fp64 sum over j != i of |m_j (x_j - x_i)| / (r^2 + eps^2)^1.5:
+    the scale against which two fp32 evaluations of a nearly cancelling sum
+    are compared. targets are ORIGINAL indices. [t] float64."""
+    pos = _f32(pos).reshape(-1, 3)
+    mass = _f32(mass).reshape(-1)
+    if targets is None:
+        nt, tp = pos.shape[0], None
+    else:
+        tgt = np.ascontiguousarray(targets, dtype=np.int64)
+        nt, tp = tgt.shape[0], _ptr(tgt)
+    out = np.zeros(nt, np.float64)
+    rc = _load().oracle_term_magnitude_f64(_ptr(pos), _ptr(mass), pos.shape[0], float(eps), tp,
+                                           nt, _ptr(out), int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle_term_magnitude_f64")
     return out
 
 

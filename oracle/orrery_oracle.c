@@ -24,8 +24,9 @@
  *
  * Precision. The pages measure single precision. Every floating-point step
  * below is one binary32 operation rounded to nearest-even: +, -, *, /, fmaf
- * (one rounding); the force term's inverse square root is itself a fixed
- * sequence of such operations (oracle_rsqrt_newton). The file is compiled
+ * (one rounding) and sqrtf (correctly rounded, as IEEE 754 requires). The
+ * force term is the law as written, m / (r2 sqrt(r2)), and nothing else: how
+ * a kernel evaluates it is that kernel's choice. The file is compiled
  * with -ffp-contract=off so the compiler adds no fused operations.
  * Where the pages leave the arithmetic open, the reading taken is written at
  * the step; the same readings are listed in the design notes.
@@ -296,10 +297,10 @@ int oracle_moments(const float *ps, const int32_t *nodes, int64_t num_nodes, int
 /* comparison is strict; a target inside an accepted cell gets no special   */
 /* case. d2 = 0 is never accepted; theta = 0 never accepts.                 */
 /*                                                                          */
-/* Term for a source (x_j, m_j), Plummer softening, G = 1:                  */
+/* Term for a source (x_j, m_j): the softened law of the workload           */
+/* definition, a = m r / (r^2 + eps^2)^(3/2), G = 1, written out plainly:   */
 /*   r2 = fl(d2 + eps2), eps2 = fl(eps * eps)                               */
-/*   y  = oracle_rsqrt_newton(r2), 1/sqrt(r2) within 2 ulp (see there)      */
-/*   f  = fl(fl(m_j * y) * fl(y * y))       (m_j r2^(-3/2))                 */
+/*   f  = fl(m_j / fl(r2 * sqrtf(r2)))      (m_j r2^(-3/2))                 */
 /*   a_ia = fmaf(f, dx_a, a_ia), in walk order                              */
 /* Cell terms use (M, CoM) with the d2 of the acceptance test.              */
 /*                                                                          */
@@ -324,49 +325,6 @@ static float cell_side_sq(float side, int level)
     return ldexpf(side * side, -2 * level);
 }
 
-/* The binary32 value nearest to 1/sqrt(x) (round to nearest; no ties can
- * occur: a midpoint between floats has 25 significant bits, and 1/m^2 of
- * such an m is never a binary32 value). A double estimate is within one ulp
- * of it; the two neighbouring midpoints m then decide exactly, since
- * 1/sqrt(x) > m  <=>  m*m*x < 1, and m*m is exact in double while fma gives
- * the sign of m*m*x - 1 exactly. Special values: +-0 -> +-inf, +inf -> +0,
- * negative or NaN -> NaN. */
-float oracle_rsqrt_rn(float x)
-{
-    if (isnan(x) || x < 0.0f) return NAN;
-    if (x == 0.0f) return copysignf(INFINITY, x);
-    if (isinf(x)) return 0.0f;
-    float y = (float)(1.0 / sqrt((double)x));
-    const double xd = (double)x;
-    float up = nextafterf(y, INFINITY);
-    double mid = 0.5 * ((double)y + (double)up);
-    if (fma(mid * mid, xd, -1.0) < 0.0) return up;
-    float down = nextafterf(y, 0.0f);
-    mid = 0.5 * ((double)y + (double)down);
-    if (fma(mid * mid, xd, -1.0) > 0.0) return down;
-    return y;
-}
-
-/* 1/sqrt(x) by a fixed binary32 recipe: the bit-level seed of C. Lomont,
- * "Fast Inverse Square Root" (2003), i.e. the integer 0x5f375a86 minus half
- * the bits of x, followed by three Newton-Raphson steps for 1/sqrt,
- * y <- y * (3/2 - (x/2) y^2), each evaluated as fl(y * fma(-h, fl(y*y), 1.5))
- * with h = fl(0.5 * x). For normal x (x >= 2^-126) the result is within
- * 2 ulp of 1/sqrt(x) (the seed is good to 3.5 %, each step squares the
- * error). Zero, subnormal and infinite x follow the same recipe and give no
- * meaningful value; r2 >= eps^2 keeps x normal whenever eps >= 1.1e-19. */
-float oracle_rsqrt_newton(float x)
-{
-    uint32_t bits;
-    memcpy(&bits, &x, sizeof bits);
-    bits = 0x5f375a86u - (bits >> 1);
-    float y;
-    memcpy(&y, &bits, sizeof y);
-    const float h = 0.5f * x;
-    for (int it = 0; it < 3; ++it) y = y * fmaf(-h, y * y, 1.5f);
-    return y;
-}
-
 static void add_term(const float xi[3], float xj, float yj, float zj, float m, float eps2,
                      float acc[3])
 {
@@ -375,8 +333,7 @@ static void add_term(const float xi[3], float xj, float yj, float zj, float m, f
     float dz = zj - xi[2];
     float d2 = fmaf(dz, dz, fmaf(dy, dy, dx * dx));
     float r2 = d2 + eps2;
-    float y = oracle_rsqrt_newton(r2);
-    float f = (m * y) * (y * y);
+    float f = m / (r2 * sqrtf(r2));
     acc[0] = fmaf(f, dx, acc[0]);
     acc[1] = fmaf(f, dy, acc[1]);
     acc[2] = fmaf(f, dz, acc[2]);
@@ -744,6 +701,65 @@ int oracle_direct_f64(const float *pos, const float *mass, int64_t n, double eps
     }
     for (int w = 0; w < threads; ++w)
         if (pthread_create(&tid[w], NULL, direct_worker, &sl[w]) != 0) return -1;
+    for (int w = 0; w < threads; ++w) pthread_join(tid[w], NULL);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The scale of a target's sum: S_i = sum over j != i of the magnitudes of   */
+/* its terms, m_j |x_j - x_i| / (|x_j - x_i|^2 + eps^2)^(3/2), in fp64.      */
+/* A sum of terms that nearly cancel (a target at the centre of a symmetric */
+/* distribution, or close unsoftened pairs) has |a_i| far below S_i; every */
+/* per-term rounding error is relative to its term, so the deviation of two */
+/* correct fp32 evaluations is bounded by a multiple of S_i, not of |a_i|.  */
+/* targets: original indices (NULL = 0..n_targets-1).                       */
+/* ------------------------------------------------------------------------ */
+static void *magnitude_worker(void *arg)
+{
+    direct_slice *d = (direct_slice *)arg;
+    for (int64_t q = d->begin; q < d->end; ++q) {
+        int64_t i = d->targets ? d->targets[q] : q;
+        double xi = d->pos[3 * i], yi = d->pos[3 * i + 1], zi = d->pos[3 * i + 2];
+        double s = 0.0;
+        for (int64_t j = 0; j < d->n; ++j) {
+            if (j == i) continue;
+            double dx = (double)d->pos[3 * j] - xi;
+            double dy = (double)d->pos[3 * j + 1] - yi;
+            double dz = (double)d->pos[3 * j + 2] - zi;
+            double d2 = dx * dx + dy * dy + dz * dz;
+            double r2 = d2 + d->eps2;
+            if (r2 > 0.0) s += fabs((double)d->mass[j]) * sqrt(d2) / (r2 * sqrt(r2));
+        }
+        d->acc[q] = s;
+    }
+    return NULL;
+}
+
+int oracle_term_magnitude_f64(const float *pos, const float *mass, int64_t n, double eps,
+                              const int64_t *targets, int64_t n_targets, double *out,
+                              int threads)
+{
+    if (threads < 1) threads = 1;
+    if (threads > 256) threads = 256;
+    if (n_targets < threads) threads = (int)(n_targets > 0 ? n_targets : 1);
+    pthread_t tid[256];
+    direct_slice sl[256];
+    for (int w = 0; w < threads; ++w) {
+        sl[w].pos = pos;
+        sl[w].mass = mass;
+        sl[w].n = n;
+        sl[w].eps2 = eps * eps;
+        sl[w].targets = targets;
+        sl[w].begin = n_targets * w / threads;
+        sl[w].end = n_targets * (w + 1) / threads;
+        sl[w].acc = out;
+    }
+    if (threads == 1) {
+        magnitude_worker(&sl[0]);
+        return 0;
+    }
+    for (int w = 0; w < threads; ++w)
+        if (pthread_create(&tid[w], NULL, magnitude_worker, &sl[w]) != 0) return -1;
     for (int w = 0; w < threads; ++w) pthread_join(tid[w], NULL);
     return 0;
 }

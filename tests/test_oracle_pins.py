@@ -184,56 +184,6 @@ def test_interleave_single_bits():
     pin_interleave_single_bits()
 
 
-def pin_rsqrt_rn():
-    """The term's inverse root is the binary32 value nearest 1/sqrt(x): checked
-    exactly with rationals (y is nearest iff the squared half-ulp midpoints on
-    either side bracket 1/x)."""
-    from fractions import Fraction
-
-    rng = np.random.default_rng(11)
-    xs = np.concatenate([
-        rng.uniform(0.0025, 100.0, 3000), 10.0 ** rng.uniform(-44, 38, 3000),
-        [1.0, 2.0, 4.0, 0.25, 3.0, 1e-45, 1.17549435e-38, 3.4028235e38, 0.0025],
-    ]).astype(np.float32)
-    for x in xs:
-        if x <= 0:
-            continue
-        y = oracle.rsqrt_rn(x)
-        up = np.nextafter(y, np.float32(np.inf))
-        down = np.nextafter(y, np.float32(0))
-        X = Fraction(float(x))
-        hi = (Fraction(float(y)) + Fraction(float(up))) / 2
-        lo = (Fraction(float(y)) + Fraction(float(down))) / 2
-        assert hi * hi * X > 1 and lo * lo * X < 1, float(x)
-    assert oracle.rsqrt_rn(0.0) == np.inf and oracle.rsqrt_rn(-0.0) == -np.inf
-    assert oracle.rsqrt_rn(np.inf) == 0.0 and np.isnan(oracle.rsqrt_rn(-1.0))
-
-
-def test_rsqrt_is_correctly_rounded():
-    pin_rsqrt_rn()
-
-
-def pin_rsqrt_newton():
-    """The force term's inverse root is within 2 ulp of 1/sqrt(x) over the
-    normal binary32 range (checked against the correctly rounded value, which
-    pin_rsqrt_rn pins to rational arithmetic)."""
-    rng = np.random.default_rng(12)
-    xs = np.concatenate([rng.uniform(0.0025, 100.0, 20000),
-                         10.0 ** rng.uniform(-37.9, 38.3, 20000),
-                         np.float32(2.0) ** np.arange(-126, 128)]).astype(np.float32)
-    worst = 0
-    for x in xs:
-        y = oracle.rsqrt_newton(x)
-        c = oracle.rsqrt_rn(x)
-        ulps = abs(int(np.float32(y).view(np.int32)) - int(np.float32(c).view(np.int32)))
-        worst = max(worst, ulps)
-    assert worst <= 2
-
-
-def test_rsqrt_newton_within_two_ulp():
-    pin_rsqrt_newton()
-
-
 def pin_quantise():
     inv = np.float32(2 ** 21)  # side 1
     assert oracle.quantise(0.0, 0.0, inv) == 0
@@ -451,6 +401,31 @@ def test_direct_f32():
     pin_direct_f32()
 
 
+def pin_term_magnitude():
+    """The tolerance scale of nearly cancelling sums: sum over j != i of
+    |m_j (x_j - x_i)| / (r^2 + eps^2)^1.5, against numpy in fp64."""
+    pos, m = uniform_cube(300, 13)
+    m = (m * np.random.default_rng(13).uniform(0.5, 2.0, 300)).astype(np.float32)
+    for eps in (0.05, 0.0):
+        x = pos.astype(np.float64)
+        d = x[None, :, :] - x[:, None, :]
+        r2 = (d * d).sum(-1)
+        np.fill_diagonal(r2, 1.0)  # the self pair is left out below
+        w = m.astype(np.float64)[None, :] * np.sqrt(r2) / (r2 + eps * eps) ** 1.5
+        np.fill_diagonal(w, 0.0)
+        ref = w.sum(1)
+        got = oracle.term_magnitude_f64(pos, m, eps)
+        assert np.abs(got - ref).max() <= 1e-12 * ref.max()
+        tg = np.array([7, 0, 299])
+        assert np.array_equal(oracle.term_magnitude_f64(pos, m, eps, tg), got[tg])
+        # never below the magnitude of the sum itself
+        assert np.all(np.linalg.norm(oracle.direct_f64(pos, m, eps), axis=1) <= got * (1 + 1e-12))
+
+
+def test_term_magnitude_against_numpy():
+    pin_term_magnitude()
+
+
 def test_direct_f64_against_numpy():
     pos, m = uniform_cube(200, 8)
     ref = direct_numpy(pos, m, EPS)
@@ -657,13 +632,12 @@ MISTAKES = [
      "return cell_side_sq(side, level) <= theta2 * d2;", pin_degenerate),
     ("last lane dropped from the union", "i < (g + 1) * width && i < n",
      "i < (g + 1) * width - 1 && i < n", pin_group_union),
-    ("two Newton steps instead of three", "for (int it = 0; it < 3; ++it) y = y * fmaf",
-     "for (int it = 0; it < 2; ++it) y = y * fmaf", pin_rsqrt_newton),
-    ("inverse root midpoint test reversed", "if (fma(mid * mid, xd, -1.0) < 0.0) return up;",
-     "if (fma(mid * mid, xd, -1.0) > 0.0) return up;", pin_rsqrt_rn),
-    ("inverse root as 1/sqrtf without correction",
-     "float y = (float)(1.0 / sqrt((double)x));\n    const double xd = (double)x;",
-     "return 1.0f / sqrtf(x);\n    float y = 0; const double xd = (double)x;", pin_rsqrt_rn),
+    ("the term's denominator r2^2 instead of r2^1.5", "float f = m / (r2 * sqrtf(r2));",
+     "float f = m / (r2 * r2);", pin_two_body),
+    ("the term's root taken of d2 instead of r2", "float f = m / (r2 * sqrtf(r2));",
+     "float f = m / (r2 * sqrtf(d2));", pin_two_body),
+    ("the term's mass left out", "float f = m / (r2 * sqrtf(r2));",
+     "float f = 1.0f / (r2 * sqrtf(r2));", pin_two_body),
     ("cell term uses the target's mass", "add_term(xi, c[0], c[1], c[2], c[3], eps2, acc);",
      "add_term(xi, c[0], c[1], c[2], t->ps[4 * i + 3], eps2, acc);", pin_far_clump),
     ("equal keys in descending index order", "if (a->index != b->index) return (a->index < b->index) ? -1 : 1;",
@@ -681,6 +655,9 @@ MISTAKES = [
      "int64_t c = nodes[4 * (k + 1) + 0];\n        while (c < node[0]) {", pin_moments),
     ("the x sum used for the y coordinate of the CoM", "cm[4 * k + 1] = (M > 0.0f) ? sy / M : 0.0f;",
      "cm[4 * k + 1] = (M > 0.0f) ? sx / M : 0.0f;", pin_moments),
+    ("the magnitude scale without the distance factor",
+     "s += fabs((double)d->mass[j]) * sqrt(d2) / (r2 * sqrt(r2));",
+     "s += fabs((double)d->mass[j]) / (r2 * sqrt(r2));", pin_term_magnitude),
     ("an opened leaf's last particle left out",
      "for (int64_t j = node[1]; j < (int64_t)node[1] + node[2]; ++j) {\n                if (j == i) continue;",
      "for (int64_t j = node[1]; j < (int64_t)node[1] + node[2] - 1; ++j) {\n                if (j == i) continue;",
