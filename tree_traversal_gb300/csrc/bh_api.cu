@@ -20,6 +20,59 @@
 #include "bh_common.cuh"
 
 namespace obh {
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int64_t node_bound(int64_t n, int32_t cap)
+{
+    return n + 21 * (n / ((int64_t)cap + 1)) + 1;
+}
+
+static int bbox_blocks_for(int64_t n)
+{
+    int64_t b = (n + 255) / 256;
+    if (b > 1216) b = 1216;  // 8 blocks per SM on 152 SMs
+    return (int)(b < 1 ? 1 : b);
+}
+
+// Lays the buffers of (n, nodes) out over one allocation; returns its size.
+// Both entry points (the grow-only workspace and the fixed no-allocation
+// scratch) lay their buffers out with this one function.
+size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
+{
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char * {
+        char *p = base ? base + off : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    b.n = n;
+    b.max_nodes = nodes;
+    b.bbox_blocks = bbox_blocks_for(n);
+    const size_t n1 = (size_t)n + 1;
+    b.bbox_partial = (float *)take(sizeof(float) * 8 * (size_t)b.bbox_blocks);
+    b.params = (DeviceParams *)take(sizeof(DeviceParams));
+    b.keys_a = (uint64_t *)take(sizeof(uint64_t) * (size_t)n);
+    b.keys_b = (uint64_t *)take(sizeof(uint64_t) * (size_t)n);
+    b.idx_a = (uint32_t *)take(sizeof(uint32_t) * (size_t)n);
+    b.idx_b = (uint32_t *)take(sizeof(uint32_t) * (size_t)n);
+    b.sort_ctl = (uint32_t *)take(sizeof(uint32_t) * (size_t)sort_ctl_words());
+    b.sort_look = (uint32_t *)take(sizeof(uint32_t) * (size_t)sort_look_words(n));
+    b.ps = (float4 *)take(sizeof(float4) * (size_t)n);
+    b.lev_d = (int8_t *)take(n1);
+    b.ncount = (uint8_t *)take(n1);
+    b.pstart = (int32_t *)take(sizeof(int32_t) * n1);
+    b.node_start = (uint32_t *)take(sizeof(uint32_t) * n1);
+    b.scan_partial = (uint32_t *)take(sizeof(uint32_t) * (size_t)scan_partial_count((int64_t)n1));
+    b.meta = (int4 *)take(sizeof(int4) * (size_t)nodes);
+    b.parent = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
+    b.nchild = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
+    b.arrive = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
+    b.sums = (float4 *)take(sizeof(float4) * (size_t)nodes);
+    b.wnode = (WalkNode *)take(sizeof(WalkNode) * ((size_t)nodes + 1));  // + the sentinel
+    return off;
+}
+
 namespace {
 
 constexpr int64_t kMaxN = int64_t(1) << 30;
@@ -111,56 +164,6 @@ std::mutex g_last_mu;  // guards g_last / g_have_last
 Workspace *g_ws[kMaxDevices] = {};
 orrery_bh_timings g_last{};
 bool g_have_last = false;
-
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-int64_t node_bound(int64_t n, int32_t cap)
-{
-    return n + 21 * (n / ((int64_t)cap + 1)) + 1;
-}
-
-int bbox_blocks_for(int64_t n)
-{
-    int64_t b = (n + 255) / 256;
-    if (b > 1216) b = 1216;  // 8 blocks per SM on 152 SMs
-    return (int)(b < 1 ? 1 : b);
-}
-
-// Lays the buffers of (n, nodes) out over one allocation; returns its size.
-size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
-{
-    size_t off = 0;
-    auto take = [&](size_t bytes) -> char * {
-        char *p = base ? base + off : nullptr;
-        off += align256(bytes);
-        return p;
-    };
-    b.n = n;
-    b.max_nodes = nodes;
-    b.bbox_blocks = bbox_blocks_for(n);
-    const size_t n1 = (size_t)n + 1;
-    b.bbox_partial = (float *)take(sizeof(float) * 8 * (size_t)b.bbox_blocks);
-    b.params = (DeviceParams *)take(sizeof(DeviceParams));
-    b.keys_a = (uint64_t *)take(sizeof(uint64_t) * (size_t)n);
-    b.keys_b = (uint64_t *)take(sizeof(uint64_t) * (size_t)n);
-    b.idx_a = (uint32_t *)take(sizeof(uint32_t) * (size_t)n);
-    b.idx_b = (uint32_t *)take(sizeof(uint32_t) * (size_t)n);
-    b.sort_ctl = (uint32_t *)take(sizeof(uint32_t) * (size_t)sort_ctl_words());
-    b.sort_look = (uint32_t *)take(sizeof(uint32_t) * (size_t)sort_look_words(n));
-    b.ps = (float4 *)take(sizeof(float4) * (size_t)n);
-    b.lev_d = (int8_t *)take(n1);
-    b.ncount = (uint8_t *)take(n1);
-    b.pstart = (int32_t *)take(sizeof(int32_t) * n1);
-    b.node_start = (uint32_t *)take(sizeof(uint32_t) * n1);
-    b.scan_partial = (uint32_t *)take(sizeof(uint32_t) * (size_t)scan_partial_count((int64_t)n1));
-    b.meta = (int4 *)take(sizeof(int4) * (size_t)nodes);
-    b.parent = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
-    b.nchild = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
-    b.arrive = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
-    b.sums = (float4 *)take(sizeof(float4) * (size_t)nodes);
-    b.wnode = (WalkNode *)take(sizeof(WalkNode) * ((size_t)nodes + 1));  // + the sentinel
-    return off;
-}
 
 void free_workspace(Workspace *w)
 {

@@ -74,6 +74,14 @@ struct Buffers {
     WalkNode *wnode;          // [max_nodes + 1] everything a walk step reads of a node, then a sentinel
 };
 
+// The node bound of n particles at leaf capacity cap: the most nodes a tree
+// can have (n leaves' worth of cells plus a chain of single-child cells of
+// length up to 21 above every cap + 1 particles), plus one.
+int64_t node_bound(int64_t n, int32_t cap);
+// Lays the buffers of one evaluation of n particles and up to `nodes` nodes
+// out over `base` (nullptr: computes the size only); returns the bytes used.
+size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes);
+
 // Kernel-launch counter (every launch site increments it).
 extern std::atomic<uint64_t> g_launches;
 

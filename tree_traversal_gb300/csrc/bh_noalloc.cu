@@ -13,9 +13,10 @@
 // The scratch is one file-scope __device__ array of kScratchBytes. Every GPU
 // on which this library's device code is loaded holds that memory until the
 // process exits. Host code may not use the array's name as a device address
-// (in host code it names a host-side shadow), so the first call on each
-// device looks the address up with cudaGetSymbolAddress while that device is
-// current, and caches it; make that first call before any stream capture.
+// (in host code it names a host-side shadow), so every call looks the
+// address up with cudaGetSymbolAddress while the caller's device is current.
+// The first call on a device may load the library's device code there (and
+// sets the kernels' attributes): make it before any stream capture.
 //
 // All calls on a device share the array and it keeps the previous call's
 // contents: every buffer that must start at zero is cleared by the call
@@ -34,72 +35,24 @@ namespace obh {
 namespace {
 
 constexpr size_t kScratchBytes = size_t(16) << 20;  // 16 MiB per device
-constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxN = int64_t(1) << 30;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_noalloc_mu;
-void *g_scratch_addr[kMaxDevices] = {};
 
-size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
-
-int64_t bound_nodes(int64_t n, int32_t cap) { return n + 21 * (n / ((int64_t)cap + 1)) + 1; }
-
-// The buffers of one evaluation laid out over `base` (nullptr: size only).
-size_t layout(Buffers &b, char *base, int64_t n, int64_t nodes)
-{
-    size_t off = 0;
-    auto take = [&](size_t bytes) -> char * {
-        char *p = base ? base + off : nullptr;
-        off += up256(bytes);
-        return p;
-    };
-    const size_t n1 = (size_t)n + 1;
-    b.n = n;
-    b.max_nodes = nodes;
-    int64_t bb = (n + 255) / 256;
-    b.bbox_blocks = (int)(bb < 1 ? 1 : (bb > 1216 ? 1216 : bb));
-    b.bbox_partial = (float *)take(sizeof(float) * 8 * (size_t)b.bbox_blocks);
-    b.params = (DeviceParams *)take(sizeof(DeviceParams));
-    b.keys_a = (uint64_t *)take(8 * (size_t)n);
-    b.keys_b = (uint64_t *)take(8 * (size_t)n);
-    b.idx_a = (uint32_t *)take(4 * (size_t)n);
-    b.idx_b = (uint32_t *)take(4 * (size_t)n);
-    b.sort_ctl = (uint32_t *)take(4 * (size_t)sort_ctl_words());
-    b.sort_look = (uint32_t *)take(4 * (size_t)sort_look_words(n));
-    b.ps = (float4 *)take(16 * (size_t)n);
-    b.lev_d = (int8_t *)take(n1);
-    b.ncount = (uint8_t *)take(n1);
-    b.pstart = (int32_t *)take(4 * n1);
-    b.node_start = (uint32_t *)take(4 * n1);
-    b.scan_partial = (uint32_t *)take(4 * (size_t)scan_partial_count((int64_t)n1));
-    b.meta = (int4 *)take(16 * (size_t)nodes);
-    b.parent = (int32_t *)take(4 * (size_t)nodes);
-    b.nchild = (int32_t *)take(4 * (size_t)nodes);
-    b.arrive = (int32_t *)take(4 * (size_t)nodes);
-    b.sums = (float4 *)take(16 * (size_t)nodes);
-    b.wnode = (WalkNode *)take(sizeof(WalkNode) * ((size_t)nodes + 1));  // + the sentinel
-    return off;
-}
-
-// Device address of this device's scratch, looked up once per device.
+// Device address of the current device's scratch. Looked up on every call
+// (cheap once the library's module is loaded on the device), so a context
+// that was torn down and created again (cudaDeviceReset) never gets a stale
+// address.
 int scratch_address(void **out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
         cudaGetLastError();
         return ORRERY_ECUDA;
     }
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return ORRERY_ECUDA;
-        }
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return ORRERY_OK;
 }
 
@@ -120,14 +73,14 @@ extern "C" int orrery_bh_forces_noalloc(const float *pos_d, const float *mass_d,
     if (n == 0) return ORRERY_OK;
     if (!pos_d || !mass_d || !acc_d) return ORRERY_EINVAL;
     Buffers b{};
-    const int64_t nodes = bound_nodes(n, leaf_cap);
-    if (nodes > (int64_t)INT32_MAX || layout(b, nullptr, n, nodes) > kScratchBytes)
+    const int64_t nodes = node_bound(n, leaf_cap);
+    if (nodes > (int64_t)INT32_MAX || carve(b, nullptr, n, nodes) > kScratchBytes)
         return ORRERY_ESCRATCH;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     void *base = nullptr;
     int rc = scratch_address(&base);
     if (rc != ORRERY_OK) return rc;
-    layout(b, (char *)base, n, nodes);
+    carve(b, (char *)base, n, nodes);
     cudaStream_t st = (cudaStream_t)stream;
     uint64_t *keys_sorted = nullptr;
     uint32_t *perm = nullptr;
