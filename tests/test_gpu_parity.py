@@ -57,13 +57,14 @@ def assert_acc_close(g, r, pos, mass, eps, caller, terms, relative=True):
     """Accelerations g (GPU) against r (oracle), rows in the same order.
 
     relative: every target within REL_TOL of |r_i| (the workloads' bar; used on
-    softened Plummer inputs). Otherwise (targets whose terms nearly cancel),
-    |g_i - r_i| <= REL_TOL * S_i * max(1, sqrt(n_i / 4096)), S_i the fp64 sum
-    of the magnitudes of the target's terms and n_i its interaction count: two
-    fp32 evaluations of the same terms differ by a few ulp per term, relative
-    to the term, and their accumulated roundings drift apart like a random
-    walk over the terms. NaN rows (coincident points without softening, where
-    the law itself is singular) must coincide."""
+    softened Plummer inputs). Otherwise (targets whose terms may nearly
+    cancel), |g_i - r_i| <= REL_TOL * max(|r_i|, S_i * max(1, sqrt(n_i / 4096))),
+    S_i the fp64 sum of the magnitudes of the particle terms j != i (the direct
+    sum's) and n_i the target's interaction count: two fp32 evaluations of the
+    same terms differ by a few ulp per term, relative to the term, and their
+    accumulated roundings drift apart like a random walk over the terms. NaN
+    rows (coincident points without softening, where the law itself is
+    singular) must coincide."""
     g64 = np.asarray(g, np.float64).reshape(-1, 3)
     r64 = np.asarray(r, np.float64).reshape(-1, 3)
     nan = np.isnan(r64).any(1)
@@ -79,7 +80,8 @@ def assert_acc_close(g, r, pos, mass, eps, caller, terms, relative=True):
         caller = np.asarray(caller, np.int64)[~nan]
         S = oracle.term_magnitude_f64(pos, mass, eps, caller)
         n_terms = np.asarray(terms, np.float64)[~nan]
-        tol = REL_TOL * S * np.maximum(1.0, np.sqrt(n_terms / 4096.0))
+        ref = np.linalg.norm(r64[~nan], axis=1)
+        tol = REL_TOL * np.maximum(ref, S * np.maximum(1.0, np.sqrt(n_terms / 4096.0)))
         worst = float((err / np.maximum(tol, 1e-300)).max(initial=0.0))
         assert np.all(err <= tol), worst
 
