@@ -5,12 +5,14 @@ radix sort, gather, octree build, moments, coherent walk, scatter) with the
 inputs already resident in device memory. Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--theta T]
-                    [--traversal coherent64|coherent|independent|...] [--term fast|exact]
-                    [--impl ours|reference] [--scaling | --crossover]
+                    [--traversal coherent64|coherent|independent|...] [--term fast|newton]
+                    [--impl ours|reference] [--scaling | --crossover | --accuracy]
 
 --scaling runs the evaluation from 1 024 to 16 777 216 particles (one JSON
 line per size); --crossover times the tree against direct summation from
-1 024 to 262 144 particles.
+1 024 to 262 144 particles; --accuracy prints the accuracy table (worst and
+RMS relative error against an fp64 direct sum) at the pages' sizes and on
+4096-target samples of the full-size workloads.
 
 --impl reference times the CPU oracle (the plain C restatement of the
 method) on this host's cores instead, on a bounded sample of the same
@@ -59,17 +61,22 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=8.0,
                    help="target wall time of the CPU-oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--term", default="fast", choices=["fast", "exact"],
-                   help="fast: the hardware approximate inverse square root (ORRERY_FAST_TERM; "
-                        "within 1e-5 of the oracle, counts identical); exact: the "
-                        "bit-reproducible Newton term (the oracle's bits). The other one is "
-                        "timed too and reported beside the headline")
+    p.add_argument("--term", default="fast", choices=["fast", "newton"],
+                   help="fast: the hardware approximate inverse square root (ORRERY_FAST_TERM); "
+                        "newton: a fixed seed and three Newton steps, reproducible bit for bit "
+                        "on an IEEE CPU. Both are within 1e-5 of the oracle's plain law with "
+                        "identical counts; the other one is timed too and reported beside the "
+                        "headline")
     p.add_argument("--scaling", action="store_true",
                    help="instead of the benchmark line, the pages' scaling study: one JSON "
                         "line per N from 1024 to 16M particles")
     p.add_argument("--crossover", action="store_true",
                    help="instead of the benchmark line, time the tree against direct "
                         "summation over a range of N (one JSON line per N)")
+    p.add_argument("--accuracy", action="store_true",
+                   help="instead of the benchmark line, the accuracy table: every target at "
+                        "4096, 16384 and 65536 particles, 4096 sampled targets at 1M and on the "
+                        "two-sphere set at theta 0.3, 0.5 and 0.7 (one JSON line per row)")
     return p.parse_args()
 
 
@@ -174,7 +181,7 @@ def run_crossover(args) -> None:
         pos_np, mass_np = plummer(n)
         pos = torch.from_numpy(pos_np).to(dev)
         mass = torch.from_numpy(mass_np).to(dev)
-        # the exact term on both sides: the direct kernel sums the same
+        # the Newton term on both sides: the direct kernel sums the same
         # particle term, so the comparison is of the algorithms alone
         t_tree = timed(lambda: tt.bh_forces(pos, mass, 0.5, 0.05, 32, args.traversal))
         walk = tt.last_timings()["walk_ms"]
@@ -182,7 +189,7 @@ def run_crossover(args) -> None:
         print(json.dumps({"n": n, "tree_ms": t_tree, "tree_walk_ms": walk, "direct_ms": t_direct,
                           "tree_speedup_vs_direct": t_direct / t_tree,
                           "direct_pairs_per_s": n * (n - 1) / (t_direct / 1000.0),
-                          "traversal": args.traversal, "term": "exact (both solvers)"}), flush=True)
+                          "traversal": args.traversal, "term": "newton (both solvers)"}), flush=True)
 
 
 def measured_peaks() -> dict:
@@ -272,26 +279,89 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def accuracy_vs_direct(pos, mass, acc, eps, count=64, seed=20260811) -> dict:
-    """Worst and RMS relative error of the accelerations against the fp64
-    direct sum on a seeded sample of targets (numpy, after the timed region;
-    the pages' accuracy table measures the same two numbers)."""
-    rng = np.random.default_rng(seed)
+def direct_f64_device(pos, mass, eps, targets, device, chunk_bytes=1 << 30):
+    """fp64 direct sum of the softened law over every j != i for the given
+    caller indices, evaluated with torch in double precision on the device
+    (the reference the accuracy figures are measured against; torch's
+    reductions sum in a tree, so the rounding of 2M terms stays near 1e-15
+    relative to their magnitude). Returns [t, 3] float64 on the host."""
+    import torch
+
+    x = torch.from_numpy(np.ascontiguousarray(pos, np.float64)).to(device)
+    m = torch.from_numpy(np.ascontiguousarray(mass, np.float64)).to(device)
+    tg = torch.from_numpy(np.asarray(targets, np.int64)).to(device)
+    n = x.shape[0]
+    per = max(1, int(chunk_bytes // (8 * 8 * max(n, 1))))
+    out = []
+    for b in range(0, tg.shape[0], per):
+        t = tg[b:b + per]
+        d = x[None, :, :] - x[t][:, None, :]
+        r2 = (d * d).sum(-1) + float(eps) * float(eps)
+        w = m[None, :] / (r2 * torch.sqrt(r2))
+        w[torch.arange(t.shape[0], device=device), t] = 0.0
+        out.append((w[:, :, None] * d).sum(1))
+    return torch.cat(out).cpu().numpy()
+
+
+def accuracy_vs_direct(pos, mass, acc, eps, device, count=4096, seed=20260811) -> dict:
+    """Worst and RMS relative error of the accelerations (caller order)
+    against the fp64 direct sum, on every target when there are at most
+    `count`, else on a seeded sample of `count` (after the timed region; the
+    pages' accuracy table measures the same two numbers)."""
     n = pos.shape[0]
-    tgt = rng.choice(n, min(n, count), replace=False)
-    x = pos.astype(np.float64)
-    m = mass.astype(np.float64)
-    errs = []
-    for i in tgt:
-        d = x - x[i]
-        r2 = (d * d).sum(1) + float(eps) * float(eps)
-        w = m / (r2 * np.sqrt(r2))
-        w[i] = 0.0
-        ref = (w[:, None] * d).sum(0)
-        errs.append(np.linalg.norm(acc[i].astype(np.float64) - ref) / np.linalg.norm(ref))
-    errs = np.asarray(errs)
+    if n <= count:
+        tgt = np.arange(n)
+    else:
+        tgt = np.sort(np.random.default_rng(seed).choice(n, count, replace=False))
+    ref = direct_f64_device(pos, mass, eps, tgt, device)
+    got = np.asarray(acc, np.float64)[tgt]
+    errs = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
     return {"vs": "fp64 direct sum", "targets": int(len(tgt)), "worst": float(errs.max()),
             "rms": float(np.sqrt(np.mean(errs * errs)))}
+
+
+# the pages' accuracy table (docs/performance/sycl_tree.md, "Accuracy"):
+# theta 0.5 against a compensated fp64 direct sum, their Plummer generator
+PAGES_ACCURACY = {4096: (2.03e-2, 2.03e-3), 16384: (1.34e-2, 1.76e-3), 65536: (7.12e-3, 1.48e-3)}
+
+
+def run_accuracy(args) -> None:
+    """One JSON line per row: the tree's accelerations (width-64 walk, both
+    force terms, and the pages' width-32 walk) against the fp64 direct sum,
+    every target at the pages' sizes and 4096 sampled targets at full size;
+    and the direct kernel at 65536 (the pages quote its RMS error too)."""
+    import torch
+
+    import tree_traversal_gb300 as tt
+    from inputs import plummer, two_spheres
+    from tree_traversal_gb300.build import build
+
+    build()
+    tt.load()
+    dev = torch.device("cuda", 0)
+    rows = [("plummer_%d" % n, plummer(n), 0.5, n) for n in (4096, 16384, 65536)]
+    rows.append(("plummer_1048576", plummer(1048576), 0.5, None))
+    two = two_spheres(1048576)
+    rows += [("two_spheres_2x1048576", two, th, None) for th in (0.3, 0.5, 0.7)]
+    for name, (pos_np, mass_np), theta, n_pages in rows:
+        pos = torch.from_numpy(pos_np).to(dev)
+        mass = torch.from_numpy(mass_np).to(dev)
+        for trav, fast in (("coherent64", True), ("coherent64", False), ("coherent", True)):
+            acc, inter, _ = tt.bh_forces(pos, mass, theta, 0.05, 32, trav, fast_term=fast)
+            # every target at the pages' sizes, 4096 sampled ones at full size
+            a = accuracy_vs_direct(pos_np, mass_np, acc.cpu().numpy(), 0.05, dev,
+                                   count=n_pages or 4096)
+            line = {"workload": name, "n": int(pos_np.shape[0]), "theta": theta, "eps": 0.05,
+                    "leaf_cap": 32, "traversal": trav, "term": "fast" if fast else "newton",
+                    **a, "interactions_per_particle": float(inter.double().sum().item()) / pos_np.shape[0]}
+            if n_pages in PAGES_ACCURACY:
+                line["pages_worst"], line["pages_rms"] = PAGES_ACCURACY[n_pages]
+            print(json.dumps(line), flush=True)
+    pos_np, mass_np = plummer(65536)
+    acc = tt.direct_forces(torch.from_numpy(pos_np).to(dev), torch.from_numpy(mass_np).to(dev), 0.05)
+    a = accuracy_vs_direct(pos_np, mass_np, acc.cpu().numpy(), 0.05, dev, count=65536)
+    print(json.dumps({"workload": "plummer_65536", "n": 65536, "solver": "direct (GPU kernel)",
+                      "eps": 0.05, **a, "pages_rms": 3.7e-6}), flush=True)
 
 
 def cpu_baseline(pos, mass, params, seconds: float) -> dict:
@@ -385,6 +455,9 @@ def main():
         return
     if args.scaling:
         run_scaling(args)
+        return
+    if args.accuracy:
+        run_accuracy(args)
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
@@ -535,8 +608,8 @@ def main():
         "config": {"workload": args.workload, "n": n, "theta": params["theta"],
                    "eps": params["eps"], "leaf_cap": params["leaf_cap"],
                    "traversal": args.traversal, "parallelism": "replicas" if world > 1 else "1gpu",
-                   "term": "fast: hardware approximate inverse root, within 1e-5 of the oracle"
-                   if fast else "exact: Newton inverse root, the oracle's bits",
+                   "term": "fast: hardware approximate inverse root" if fast
+                   else "newton: fixed seed and three Newton steps (bit-reproducible on an IEEE CPU)",
                    "l2": "flushed between steps (256 MiB write outside the step events)"},
         "gpu_launches": int(launches),
         "clocks": {"sm_mhz": csum["sm_mhz"], "sm_max_mhz": csum["sm_max_mhz"],
@@ -579,11 +652,11 @@ def main():
                          "visits": vis_mean, "visits_" + other: vis_other,
                          "redundancy": (vis_mean / vis_other) if args.traversal != "independent"
                          else (vis_other / vis_mean)},
-        ("exact_term" if fast else "fast_term"): {
+        ("newton_term" if fast else "fast_term"): {
             "ms_per_step": statistics.fmean(other_ms), "walk_ms": statistics.fmean(other_walk),
             "value": interactions / (statistics.fmean(other_ms) / 1000.0)},
         "comparison_traversals": comparison,
-        "accuracy": accuracy_vs_direct(pos_np, mass_np, h_out[0].numpy(), params["eps"]),
+        "accuracy": accuracy_vs_direct(pos_np, mass_np, h_out[0].numpy(), params["eps"], device),
         "redundancy_width32": (comparison["coherent"]["visits_per_particle"] / vis_other)
         if "coherent" in comparison and args.traversal != "independent" else None,
     }

@@ -81,7 +81,7 @@ def test_noalloc_every_traversal(lib):
 
 def test_noalloc_documented_sizes_fit(lib):
     """The header's promise: every n up to 65 536 fits at leaf_cap 16 and up to
-    80 000 at leaf_cap 32 (the layout's limits are 75 827 and 95 488). At both
+    80 000 at leaf_cap 32 (the layout's limits are 79 030 and 99 197). At both
     limits the results are checked against the oracle itself: counts bit for
     bit, accelerations within 1e-5 relative error."""
     import oracle

@@ -66,7 +66,6 @@ size_t carve(Buffers &b, char *base, int64_t n, int64_t nodes)
     b.scan_partial = (uint32_t *)take(sizeof(uint32_t) * (size_t)scan_partial_count((int64_t)n1));
     b.meta = (int4 *)take(sizeof(int4) * (size_t)nodes);
     b.parent = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
-    b.nchild = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
     b.arrive = (int32_t *)take(sizeof(int32_t) * (size_t)nodes);
     b.sums = (float4 *)take(sizeof(float4) * (size_t)nodes);
     b.wnode = (WalkNode *)take(sizeof(WalkNode) * ((size_t)nodes + 1));  // + the sentinel
@@ -289,7 +288,7 @@ void run_tree(Workspace &w, const float *pos, const float *mass, int32_t cap, cu
     record_event(w.ev[EV_GATHER], st);
     launch_build(*keys_sorted, cap, b, st);
     record_event(w.ev[EV_BUILD], st);
-    launch_moments(b, st);
+    launch_moments(cap, b, st);
     record_event(w.ev[EV_MOMENTS], st);
 }
 

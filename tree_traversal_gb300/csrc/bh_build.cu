@@ -75,16 +75,15 @@ k_build_levels(const uint64_t *__restrict__ K, int64_t n, int32_t cap,
 }
 
 // Writes the nodes that start at each position: their first particle and
-// level, the parent index (the first node's parent is the level-D cell found
-// by k_build_levels, every later one's is the node before it: the cells
-// starting at one position are nested), and counts children with an atomic
-// add on the parent. The cells' ends come from k_build_ends, one node per
-// thread, so no thread walks a chain of searches.
+// level, and the parent index (the first node's parent is the level-D cell
+// found by k_build_levels, every later one's is the node before it: the
+// cells starting at one position are nested). The cells' ends come from
+// k_build_ends, one node per thread, so no thread walks a chain of searches.
 __global__ void __launch_bounds__(kThreads)
 k_build_emit(int64_t n, const int8_t *__restrict__ lev_d, const uint8_t *__restrict__ ncount,
              const int32_t *__restrict__ pstart, const uint32_t *__restrict__ node_start,
              int64_t max_nodes, int4 *__restrict__ meta, int32_t *__restrict__ parent,
-             int32_t *__restrict__ nchild, DeviceParams *P)
+             DeviceParams *P)
 {
     if (P->status & kStatusInternal) return;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -113,38 +112,17 @@ k_build_emit(int64_t n, const int8_t *__restrict__ lev_d, const uint8_t *__restr
         const int64_t k = (int64_t)base + j;
         meta[k] = make_int4(0, (int)i, 0, first_level + j);  // escape and count: k_build_ends
         parent[k] = par;
-        if (par >= 0) atomicAdd(&nchild[par], 1);
         par = (int32_t)k;
     }
     atomicMax(&P->depth, first_level + cnt - 1);
 }
 
-// One thread per node: the end of its cell (the first position past the
-// keys that share the node's top L octal digits; a binary search over the
-// sorted keys), hence its particle count and escape index (the node index at
-// that position), and the node's walk record {escape, the node a target that
-// does not accept it goes to next (escape for a leaf, which it opens; k + 1
-// for an internal node, which it enters), leaf count (0 for an internal
-// node), bits of (side 2^-level)^2}. Every node k < num_nodes gets its record
-// here, and every record's next nodes are checked to lie in (k, num_nodes]:
-// so a walk's node index strictly increases and every walk ends within
-// num_nodes steps (an escape outside that range is flagged and replaced by
-// num_nodes).
-__global__ void __launch_bounds__(kThreads)
-k_build_ends(const uint64_t *__restrict__ K, int64_t n, const uint32_t *__restrict__ node_start,
-             int64_t max_nodes, int32_t leaf_cap, int4 *__restrict__ meta,
-             WalkNode *__restrict__ wnode, DeviceParams *P)
+__device__ __forceinline__ void node_end(const uint64_t *__restrict__ K, int64_t n,
+                                         const uint32_t *__restrict__ node_start, int64_t total,
+                                         int32_t leaf_cap, int4 *__restrict__ meta,
+                                         WalkNode *__restrict__ wnode, int32_t *__restrict__ arrive,
+                                         DeviceParams *P, int64_t k)
 {
-    if (P->status & kStatusInternal) return;
-    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t total = node_start[n];
-    if (k == 0 && total <= max_nodes) {
-        // a sentinel after the last node: a leaf no target accepts (side^2 =
-        // +inf) with zero mass, where the packed walk's group ends
-        wnode[total].w = make_int4((int)total, (int)total, 1, 0x7f800000);
-        wnode[total].c = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    }
-    if (k >= total || total > max_nodes) return;
     const int4 m = meta[k];
     const int64_t i = m.y;
     const int L = m.w;
@@ -173,9 +151,41 @@ k_build_ends(const uint64_t *__restrict__ K, int64_t n, const uint32_t *__restri
     const int count = (int)(end - i);
     const bool leaf = count <= leaf_cap || L == kLevels;
     meta[k] = make_int4(esc, (int)i, count, L);
+    arrive[k] = 0;
     wnode[k].w = make_int4(esc, leaf ? esc : (int)k + 1, leaf ? count : 0, __float_as_int(P->s2[L]));
 }
 
+// One thread per node (a grid-stride loop over the node count the scan
+// produced, so the grid follows the tree rather than its bound): the end of
+// its cell (the first position past the keys that share the node's top L
+// octal digits; a binary search over the sorted keys), hence its particle
+// count and escape index (the node index at that position), and the node's
+// walk record {escape, the node a target that does not accept it goes to
+// next (escape for a leaf, which it opens; k + 1 for an internal node, which
+// it enters), leaf count (0 for an internal node), bits of (side
+// 2^-level)^2}. Every node k < num_nodes gets its record here, and every
+// record's next nodes are checked to lie in (k, num_nodes]: so a walk's node
+// index strictly increases and every walk ends within num_nodes steps (an
+// escape outside that range is flagged and replaced by num_nodes). The
+// node's arrival count for the moments climb is cleared here too.
+__global__ void __launch_bounds__(kThreads)
+k_build_ends(const uint64_t *__restrict__ K, int64_t n, const uint32_t *__restrict__ node_start,
+             int64_t max_nodes, int32_t leaf_cap, int4 *__restrict__ meta,
+             WalkNode *__restrict__ wnode, int32_t *__restrict__ arrive, DeviceParams *P)
+{
+    if (P->status & kStatusInternal) return;
+    const int64_t total = node_start[n];
+    if (total > max_nodes) return;
+    const int64_t first_k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (first_k == 0) {
+        // a sentinel after the last node: a leaf no target accepts (side^2 =
+        // +inf) with zero mass, where the packed walk's group ends
+        wnode[total].w = make_int4((int)total, (int)total, 1, 0x7f800000);
+        wnode[total].c = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    for (int64_t k = first_k; k < total; k += (int64_t)gridDim.x * blockDim.x)
+        node_end(K, n, node_start, total, leaf_cap, meta, wnode, arrive, P, k);
+}
 // A node whose mass is not finite or whose CoM lies at 2^126 or beyond is
 // reported as non-finite: with every coordinate below 2^125 (checked with the
 // bounding box), every separation the walks form is then a finite number.
@@ -203,45 +213,57 @@ __device__ __forceinline__ void store_node(int64_t k, float sx, float sy, float 
     wnode[k].c = store_moments(k, sx, sy, sz, M, sums, P);
 }
 
-// a6: one thread per leaf (the last node of each position's chain) sums its
-// particles in sorted order, then climbs: the last child to arrive at a
-// parent (atomic arrival count == child count) sums all of the parent's
-// children in child order. No thread ever waits for another.
-__global__ void __launch_bounds__(kThreads)
-k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ ncount,
-          const uint32_t *__restrict__ node_start, const int4 *__restrict__ meta,
-          const int32_t *__restrict__ parent, const int32_t *__restrict__ nchild,
-          int32_t *__restrict__ arrive, float4 *sums, WalkNode *__restrict__ wnode,
-          DeviceParams *P)
+// a6: one thread per leaf (a grid-stride loop over the nodes) sums its
+// particles in sorted order, then climbs: each child adds its particle count
+// to its parent's arrival count, and the child that completes it (the
+// children's ranges partition the parent's, so their counts add up to the
+// parent's) sums all of the parent's children in child order. No thread
+// ever waits for another.
+__device__ __forceinline__ void leaf_and_climb(const float4 *__restrict__ ps, int64_t n,
+                                               const int4 *__restrict__ meta,
+                                               const int32_t *__restrict__ parent,
+                                               int32_t *__restrict__ arrive, float4 *sums,
+                                               WalkNode *__restrict__ wnode, DeviceParams *P,
+                                               int total, int64_t k, int4 m)
 {
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const int cnt = ncount[i];
-    if (cnt == 0 || (P->status & (kStatusNodeBound | kStatusInternal))) return;
-    int64_t k = (int64_t)node_start[i] + cnt - 1;
-    const int4 m = meta[k];
     if (m.y < 0 || m.z < 0 || (int64_t)m.y + m.z > n) {
         atomicOr((int *)&P->status, kStatusInternal);
         return;
     }
-    const int total = P->num_nodes;
     float M = 0.0f, sx = 0.0f, sy = 0.0f, sz = 0.0f;
-    for (int64_t j = m.y; j < (int64_t)m.y + m.z; ++j) {
-        const float4 p = __ldg(ps + j);
-        M = __fadd_rn(M, p.w);
-        sx = __fmaf_rn(p.w, p.x, sx);
-        sy = __fmaf_rn(p.w, p.y, sy);
-        sz = __fmaf_rn(p.w, p.z, sz);
+    const float4 *src = ps + m.y;
+    int j = 0;
+    // four loads in flight, then the additions in order
+    for (; j + 4 <= m.z; j += 4) {
+        float4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) q[u] = __ldg(src + j + u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            M = __fadd_rn(M, q[u].w);
+            sx = __fmaf_rn(q[u].w, q[u].x, sx);
+            sy = __fmaf_rn(q[u].w, q[u].y, sy);
+            sz = __fmaf_rn(q[u].w, q[u].z, sz);
+        }
+    }
+    for (; j < m.z; ++j) {
+        const float4 q = __ldg(src + j);
+        M = __fadd_rn(M, q.w);
+        sx = __fmaf_rn(q.w, q.x, sx);
+        sy = __fmaf_rn(q.w, q.y, sy);
+        sz = __fmaf_rn(q.w, q.z, sz);
     }
     store_node(k, sx, sy, sz, M, sums, wnode, P);
+    int carried = m.z;
     int64_t node = parent[k];
     while (node >= 0) {
-        // release: this child's sums before the count; acquire: the last
-        // child to arrive sees every sibling's sums
+        // release: this child's sums before the count; acquire: the child
+        // that completes the count sees every sibling's sums
         cuda::atomic_ref<int32_t, cuda::thread_scope_device> count(arrive[node]);
-        const int prev = count.fetch_add(1, cuda::std::memory_order_acq_rel);
-        if (prev != nchild[node] - 1) return;
-        const int esc = meta[node].x;
+        const int prev = count.fetch_add(carried, cuda::std::memory_order_acq_rel);
+        const int4 pm = meta[node];
+        if (prev + carried != pm.z) return;
+        const int esc = pm.x;
         M = sx = sy = sz = 0.0f;
         if (esc > total) {
             atomicOr((int *)&P->status, kStatusInternal);
@@ -261,11 +283,37 @@ k_moments(const float4 *__restrict__ ps, int64_t n, const uint8_t *__restrict__ 
             c = nc;
         }
         store_node(node, sx, sy, sz, M, sums, wnode, P);
+        carried = pm.z;
         node = parent[node];
     }
 }
 
+__global__ void __launch_bounds__(kThreads)
+k_moments(const float4 *__restrict__ ps, int64_t n, int32_t leaf_cap,
+          const int4 *__restrict__ meta, const int32_t *__restrict__ parent,
+          int32_t *__restrict__ arrive, float4 *sums, WalkNode *__restrict__ wnode,
+          DeviceParams *P)
+{
+    if (P->status & (kStatusNodeBound | kStatusInternal)) return;
+    const int total = P->num_nodes;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total;
+         k += (int64_t)gridDim.x * blockDim.x) {
+        const int4 m = meta[k];
+        if (m.z <= leaf_cap || m.w == kLevels)  // a leaf
+            leaf_and_climb(ps, n, meta, parent, arrive, sums, wnode, P, total, k, m);
+    }
+}
+
 }  // namespace
+
+// Grid of the kernels that loop over the nodes: the node count is only
+// known on the device, so they stride over it with at most a few waves of
+// blocks (and no more blocks than the bound needs).
+static unsigned node_grid(const Buffers &b)
+{
+    const unsigned want = ceil_div(b.max_nodes, kThreads);
+    return want < 152u * 8u ? want : 152u * 8u;
+}
 
 void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b,
                   cudaStream_t st)
@@ -275,22 +323,17 @@ void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &
     g_launches += 1;
     // node_start = exclusive scan of ncount over n + 1 entries
     launch_scan_u8(b.ncount, b.node_start, b.n + 1, b.scan_partial, st);
-    cudaMemsetAsync(b.nchild, 0, sizeof(int32_t) * (size_t)b.max_nodes, st);
     k_build_emit<<<ceil_div(b.n, kThreads), kThreads, 0, st>>>(
-        b.n, b.lev_d, b.ncount, b.pstart, b.node_start, b.max_nodes, b.meta, b.parent, b.nchild,
-        b.params);
-    // the node count is only known on the device: cover the bound
-    k_build_ends<<<ceil_div(b.max_nodes, kThreads), kThreads, 0, st>>>(
-        keys_sorted, b.n, b.node_start, b.max_nodes, leaf_cap, b.meta, b.wnode, b.params);
+        b.n, b.lev_d, b.ncount, b.pstart, b.node_start, b.max_nodes, b.meta, b.parent, b.params);
+    k_build_ends<<<node_grid(b), kThreads, 0, st>>>(keys_sorted, b.n, b.node_start, b.max_nodes,
+                                                   leaf_cap, b.meta, b.wnode, b.arrive, b.params);
     g_launches += 2;
 }
 
-void launch_moments(const Buffers &b, cudaStream_t st)
+void launch_moments(int32_t leaf_cap, const Buffers &b, cudaStream_t st)
 {
-    cudaMemsetAsync(b.arrive, 0, sizeof(int32_t) * (size_t)b.max_nodes, st);
-    k_moments<<<ceil_div(b.n, kThreads), kThreads, 0, st>>>(b.ps, b.n, b.ncount, b.node_start,
-                                                           b.meta, b.parent, b.nchild, b.arrive,
-                                                           b.sums, b.wnode, b.params);
+    k_moments<<<node_grid(b), kThreads, 0, st>>>(b.ps, b.n, leaf_cap, b.meta, b.parent, b.arrive,
+                                                b.sums, b.wnode, b.params);
     g_launches += 1;
 }
 

@@ -67,8 +67,7 @@ struct Buffers {
     uint32_t *scan_partial;   // scan block sums
     int4 *meta;               // [max_nodes] {escape, first, count, level}
     int32_t *parent;          // [max_nodes]
-    int32_t *nchild;          // [max_nodes]
-    int32_t *arrive;          // [max_nodes]
+    int32_t *arrive;          // [max_nodes] particles of the children summed so far (moments)
     // a6
     float4 *sums;             // [max_nodes] {S_x, S_y, S_z, M}
     WalkNode *wnode;          // [max_nodes + 1] everything a walk step reads of a node, then a sentinel
@@ -93,7 +92,7 @@ void launch_gather(const float *pos, const float *mass, const uint32_t *perm, co
                    cudaStream_t st);
 void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b,
                   cudaStream_t st);
-void launch_moments(const Buffers &b, cudaStream_t st);
+void launch_moments(int32_t leaf_cap, const Buffers &b, cudaStream_t st);
 // a7 with the a8 scatter fused: results land in the caller's order. Walks
 // the sorted targets [t_begin, t_end) against the whole tree.
 void launch_walk(int traversal, float theta, float eps, const uint32_t *perm, const Buffers &b,

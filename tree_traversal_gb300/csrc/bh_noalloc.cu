@@ -20,8 +20,8 @@
 //
 // All calls on a device share the array and it keeps the previous call's
 // contents: every buffer that must start at zero is cleared by the call
-// itself (the child and arrival counters are reset with cudaMemsetAsync, the
-// status word by the cube kernel). Two calls whose GPU work overlapped would
+// itself (the moments' arrival counters by the build, the status word by the
+// cube kernel). Two calls whose GPU work overlapped would
 // race on the array; this entry point serialises its calls with a lock and
 // waits for its own work before returning, so its own calls never overlap.
 // It does not share the array with orrery_bh_forces, whose workspace is
@@ -89,7 +89,7 @@ extern "C" int orrery_bh_forces_noalloc(const float *pos_d, const float *mass_d,
     launch_sort(b, st, &keys_sorted, &perm);
     launch_gather(pos_d, mass_d, perm, b, st);
     launch_build(keys_sorted, leaf_cap, b, st);
-    launch_moments(b, st);
+    launch_moments(leaf_cap, b, st);
     launch_walk(traversal, theta, eps, perm, b, 0, n, acc_d, interactions_d, visits_d, st);
     int status = 0;
     cudaMemcpyAsync(&status, &b.params->status, sizeof(int), cudaMemcpyDeviceToHost, st);
