@@ -206,7 +206,8 @@ WALK_KERNELS = {"coherent": "k_walk_coherent", "coherent16": "k_walk_coherent",
                 "ballot": "k_walk_coherent", "coherent64": "k_walk_paired",
                 "together": "k_walk_together", "independent": "k_walk_independent"}
 TRAFFIC_PROFILES = {("k_walk_paired", True): "walk_paired_fast_plummer_1m.md",
-                    ("k_walk_coherent", False): "walk_coherent_plummer_1m.md"}
+                    ("k_walk_coherent", True): "walk_coherent_plummer_1m.md",
+                    ("k_walk_independent", True): "walk_independent_plummer_1m.md"}
 
 
 def profile_traffic(kernel_src: str, kernel: str, fast: bool) -> float | None:

@@ -13,9 +13,11 @@ WALK_SRC = os.path.join(ROOT, "tree_traversal_gb300", "csrc", "bh_walk.cu")
 
 
 def test_committed_traffic_matches_the_current_walk_source():
-    # the summary the default bench line reads was captured on this source
-    traffic = bench.profile_traffic(WALK_SRC, "k_walk_paired", True)
-    assert traffic is not None and 40e6 < traffic < 120e6
+    # the summaries the bench lines read were captured on this source: the
+    # default width-64 walk and the two walks the pages compare
+    for kernel in ("k_walk_paired", "k_walk_coherent", "k_walk_independent"):
+        traffic = bench.profile_traffic(WALK_SRC, kernel, True)
+        assert traffic is not None and 40e6 < traffic < 120e6, kernel
 
 
 def test_traffic_is_withheld_for_a_changed_source(tmp_path):
@@ -25,4 +27,4 @@ def test_traffic_is_withheld_for_a_changed_source(tmp_path):
         f.write("\n// changed\n")
     assert bench.profile_traffic(str(changed), "k_walk_paired", True) is None
     # and for a walk kernel with no summary of its own
-    assert bench.profile_traffic(WALK_SRC, "k_walk_independent", True) is None
+    assert bench.profile_traffic(WALK_SRC, "k_walk_together", True) is None
