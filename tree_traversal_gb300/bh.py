@@ -52,8 +52,9 @@ def bh_forces(pos: torch.Tensor, mass: torch.Tensor, theta: float = 0.5, eps: fl
     particle-particle} or None, visits [n] int32 or None); the counters are
     uint32 values stored in int32 tensors (they never exceed 2^31).
     ``out`` may pass preallocated (acc, interactions, visits) tensors.
-    ``fast_term`` selects the approximate inverse square root (ORRERY_FAST_TERM):
-    faster, equal to the exact path to rounding rather than bit for bit.
+    ``fast_term`` selects the hardware approximate inverse square root
+    (ORRERY_FAST_TERM) instead of the fixed Newton sequence: faster; both are
+    within the same tolerance of the law, and the counts are identical.
     ``targets`` = (begin, end) walks only the sorted targets [begin, end)
     (orrery_bh_forces_range): only their entries of the outputs are written."""
     n = int(pos.shape[0]) if pos.dim() == 2 else -1

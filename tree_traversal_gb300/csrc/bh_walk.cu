@@ -17,11 +17,13 @@
 //   accept iff (side 2^-L)^2 < theta^2 |CoM_k - x_i|^2  -> cell term, escape
 //   else if k is a leaf -> particle terms over its particles j != i, escape
 //   else -> k + 1 (first child)
-// Term: r2 = d2 + eps^2, y = rsqrt_newton(r2), f = (m y)(y y), a += f
-// (x_src - x_i) by fused multiply-add. Every floating-point step is one
-// correctly rounded binary32 operation (explicit _rn intrinsics), so
-// decisions and sums do not depend on contraction choices, and a CPU
-// restatement of the same steps reproduces them bit for bit.
+// Term (the softened law a = m r / (r^2 + eps^2)^(3/2)): r2 = d2 + eps^2,
+// y = 1/sqrt(r2) (a fixed Newton sequence, or the hardware approximation
+// with the fast-term flag), f = (m y)(y y), a += f (x_src - x_i) by fused
+// multiply-add, in walk order. Every floating-point step is one correctly
+// rounded binary32 operation (explicit _rn intrinsics), so decisions and sums
+// do not depend on contraction choices: a CPU restatement of the decisions
+// reproduces the counts bit for bit, and of the Newton term the sums.
 //
 // GB300 shape of the coherent kernels: the node k is group-uniform, so its
 // 32-byte record (one sector) is read once per group step and broadcast. The
