@@ -210,17 +210,31 @@ TRAFFIC_PROFILES = {("k_walk_paired", True): "walk_paired_fast_plummer_1m.md",
                     ("k_walk_independent", True): "walk_independent_plummer_1m.md"}
 
 
+def code_sha256(path: str) -> str:
+    """SHA-256 of a CUDA source with its // comments, trailing blanks and
+    empty lines removed: changes to comments leave it (and the compiled
+    kernel) unchanged, any change to the code changes it."""
+    import re
+
+    lines = []
+    for line in open(path, encoding="utf-8"):
+        line = re.sub(r"//.*$", "", line.rstrip("\n")).rstrip()
+        if line.strip():
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def profile_traffic(kernel_src: str, kernel: str, fast: bool) -> float | None:
     """Per-launch DRAM bytes of the walk kernel from the committed ncu summary,
-    only while the kernel source is the one that was profiled."""
+    only while the kernel's code is the code that was profiled."""
     name = TRAFFIC_PROFILES.get((kernel, fast))
     path = os.path.join(ROOT, "profiles", name) if name else ""
     if not name or not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    sha = code_sha256(kernel_src)
     found_sha, traffic = None, None
     for line in open(path):
-        if line.startswith("kernel_source_sha256:"):
+        if line.startswith("kernel_code_sha256:"):
             found_sha = line.split(":", 1)[1].strip()
         if line.startswith("dram_bytes_per_launch_full_size:"):
             traffic = float(line.split(":", 1)[1].strip())

@@ -1,6 +1,6 @@
 """bench.py's host-side bookkeeping, on the CPU: the walk's DRAM traffic is
-taken from the committed ncu summary only while the profiled kernel source
-is the current one."""
+taken from the committed ncu summary only while the profiled kernel code (the
+source without its comments) is the current one."""
 from __future__ import annotations
 
 import os
@@ -20,11 +20,18 @@ def test_committed_traffic_matches_the_current_walk_source():
         assert traffic is not None and 40e6 < traffic < 120e6, kernel
 
 
-def test_traffic_is_withheld_for_a_changed_source(tmp_path):
+def test_traffic_is_withheld_for_changed_code(tmp_path):
+    # a comment changes nothing the kernel does: the summary still applies
+    commented = tmp_path / "commented.cu"
+    shutil.copy(WALK_SRC, commented)
+    with open(commented, "a") as f:
+        f.write("\n// a comment\n\n")
+    assert bench.profile_traffic(str(commented), "k_walk_paired", True) is not None
+    # a change to the code withholds it
     changed = tmp_path / "bh_walk.cu"
     shutil.copy(WALK_SRC, changed)
     with open(changed, "a") as f:
-        f.write("\n// changed\n")
+        f.write("\nstatic int changed_code = 1;\n")
     assert bench.profile_traffic(str(changed), "k_walk_paired", True) is None
     # and for a walk kernel with no summary of its own
     assert bench.profile_traffic(WALK_SRC, "k_walk_together", True) is None
