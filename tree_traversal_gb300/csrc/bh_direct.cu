@@ -6,8 +6,10 @@
 //
 // a_i = sum over j != i, in caller order j = 0, 1, ..., of the term
 // r2 = d2 + eps^2, y = rsqrt_newton(r2), f = (m_j y)(y y), a_i += f (x_j - x_i)
-// -- the tree walk's particle term, so a CPU restatement reproduces every
-// bit. Two targets per thread (i and i + kThreads within a block's 2 kThreads
+// -- the tree walk's particle term with its Newton inverse root: a fixed
+// sequence of binary32 operations, so a CPU that repeats it reproduces every
+// bit, and within a few ulp per term of the law evaluated plainly. Two
+// targets per thread (i and i + kThreads within a block's 2 kThreads
 // targets), both summed in packed float2 instructions (__fadd2_rn,
 // __fmul2_rn, __ffma2_rn round each component exactly as the scalar forms),
 // so one instruction issue does two pairs' arithmetic. Sources are staged
