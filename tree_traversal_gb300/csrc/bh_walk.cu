@@ -161,6 +161,31 @@ __device__ __forceinline__ void particle_term(const float4 &p, const float4 &xi,
     add_term<kFast, kNormal>(dx, dy, dz, dist2(dx, dy, dz), p.w, eps2, ax, ay, az);
 }
 
+// The same two functions for one target with its x and y components in one
+// packed pair (__fadd2_rn and __ffma2_rn round each component exactly like
+// the scalar forms, and d2 keeps its sequential order): the same results bit
+// for bit, in two fewer instructions per term. nxy = (-x_i, -y_i): a
+// separation is then one packed add.
+template <bool kFast, bool kNormal = false>
+__device__ __forceinline__ void add_term_xy(float2 dxy, float dz, float d2, float m, float eps2,
+                                            float2 &axy, float &az)
+{
+    const float r2 = __fadd_rn(d2, eps2);
+    const float y = inv_sqrt<kFast, kNormal>(r2);
+    const float f = __fmul_rn(__fmul_rn(m, y), __fmul_rn(y, y));
+    axy = __ffma2_rn(make_float2(f, f), dxy, axy);
+    az = __fmaf_rn(f, dz, az);
+}
+
+template <bool kFast, bool kNormal = false>
+__device__ __forceinline__ void particle_term_xy(const float4 &p, float2 nxy, float z, float eps2,
+                                                 float2 &axy, float &az)
+{
+    const float2 dxy = __fadd2_rn(make_float2(p.x, p.y), nxy);
+    const float dz = __fsub_rn(p.z, z);
+    add_term_xy<kFast, kNormal>(dxy, dz, dist2(dxy.x, dxy.y, dz), p.w, eps2, axy, az);
+}
+
 // Block prologue shared by both kernels: status, node count and whether the
 // self term may be summed (see the file comment). Returns false to skip.
 template <bool kFast>
@@ -218,8 +243,10 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
     const int tgt = a.t_begin + blockIdx.x * blockDim.x + threadIdx.x;
     const bool valid = tgt < a.t_end;
     const float4 xi = valid ? __ldg(a.ps + tgt) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const float2 nxy = make_float2(-xi.x, -xi.y);
     int next = valid ? 0 : num_nodes;
-    float ax = 0.0f, ay = 0.0f, az = 0.0f;
+    float2 axy = make_float2(0.0f, 0.0f);
+    float az = 0.0f;
     uint32_t pc = 0, pp = 0;
     int steps = 0;
     int kb = __any_sync(gmask, valid) ? 0 : num_nodes;  // the ballot form's node
@@ -231,12 +258,11 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
         const float4 c = kLocal ? loc.nodes[k].c : __ldg(&a.wnode[k].c);
         bool open = false, descend = false;
         if (next == k) {
-            const float dx = __fsub_rn(c.x, xi.x);
-            const float dy = __fsub_rn(c.y, xi.y);
+            const float2 dxy = __fadd2_rn(make_float2(c.x, c.y), nxy);
             const float dz = __fsub_rn(c.z, xi.z);
-            const float d2 = dist2(dx, dy, dz);
+            const float d2 = dist2(dxy.x, dxy.y, dz);
             if (__int_as_float(w.w) < __fmul_rn(a.theta2, d2)) {
-                add_term<kFast, kSelfFree>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
+                add_term_xy<kFast, kSelfFree>(dxy, dz, d2, c.w, a.eps2, axy, az);
                 if (kCount) ++pc;
                 next = w.x;
             } else {
@@ -260,7 +286,7 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
 #pragma unroll 4
                     for (int j = 0; j < count; ++j)
                         if (kSelfFree || j != self)
-                            particle_term<kFast, kSelfFree>(loc.ps[first + j], xi, a.eps2, ax, ay, az);
+                            particle_term_xy<kFast, kSelfFree>(loc.ps[first + j], nxy, xi.z, a.eps2, axy, az);
                 }
                 continue;
             }
@@ -272,11 +298,11 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
                     if (kSelfFree) {
 #pragma unroll 4
                         for (int j = 0; j < chunk; ++j)
-                            particle_term<kFast, kSelfFree>(stage[j], xi, a.eps2, ax, ay, az);
+                            particle_term_xy<kFast, kSelfFree>(stage[j], nxy, xi.z, a.eps2, axy, az);
                     } else {
                         const int self = tgt - (first + b);
                         for (int j = 0; j < chunk; ++j)
-                            if (j != self) particle_term<kFast, kSelfFree>(stage[j], xi, a.eps2, ax, ay, az);
+                            if (j != self) particle_term_xy<kFast, kSelfFree>(stage[j], nxy, xi.z, a.eps2, axy, az);
                     }
                 }
                 __syncwarp(gmask);
@@ -284,7 +310,7 @@ __device__ __forceinline__ void coherent_walk(const WalkArgs &a, int num_nodes, 
         }
     }
     if (steps > num_nodes && glane == 0) atomicOr(&a.P->status, kStatusWalkBound);
-    if (valid) store_target<kCount>(a, tgt, ax, ay, az, pc, pp, steps);  // every step visits the union
+    if (valid) store_target<kCount>(a, tgt, axy.x, axy.y, az, pc, pp, steps);  // every step visits the union
 }
 
 template <int W, bool kCount, bool kBallot, bool kFast>
@@ -622,18 +648,19 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
     const int t = a.t_begin + blockIdx.x * kThreads + threadIdx.x;
     if (t >= a.t_end) return;
     const float4 xi = __ldg(a.ps + t);
-    float ax = 0.0f, ay = 0.0f, az = 0.0f;
+    const float2 nxy = make_float2(-xi.x, -xi.y);
+    float2 axy = make_float2(0.0f, 0.0f);
+    float az = 0.0f;
     uint32_t pc = 0, pp = 0;
     int k = 0, steps = 0;
     for (; k < num_nodes; ++steps) {
         const int4 w = __ldg(&a.wnode[k].w);
         const float4 c = __ldg(&a.wnode[k].c);
-        const float dx = __fsub_rn(c.x, xi.x);
-        const float dy = __fsub_rn(c.y, xi.y);
+        const float2 dxy = __fadd2_rn(make_float2(c.x, c.y), nxy);
         const float dz = __fsub_rn(c.z, xi.z);
-        const float d2 = dist2(dx, dy, dz);
+        const float d2 = dist2(dxy.x, dxy.y, dz);
         if (__int_as_float(w.w) < __fmul_rn(a.theta2, d2)) {
-            add_term<kFast, kSelfFree>(dx, dy, dz, d2, c.w, a.eps2, ax, ay, az);
+            add_term_xy<kFast, kSelfFree>(dxy, dz, d2, c.w, a.eps2, axy, az);
             if (kCount) ++pc;
             k = w.x;
         } else if (w.z != 0) {
@@ -644,14 +671,14 @@ __device__ __forceinline__ void independent_walk(const WalkArgs &a, int num_node
             }
             if (kCount) pp += count - ((unsigned)(t - first) < (unsigned)count ? 1u : 0u);
             for (int j = first; j < first + count; ++j)
-                if (kSelfFree || j != t) particle_term<kFast, kSelfFree>(__ldg(a.ps + j), xi, a.eps2, ax, ay, az);
+                if (kSelfFree || j != t) particle_term_xy<kFast, kSelfFree>(__ldg(a.ps + j), nxy, xi.z, a.eps2, axy, az);
             k = w.x;
         } else {
             k = k + 1;
         }
     }
     if (k < num_nodes) atomicOr(&a.P->status, kStatusWalkBound);
-    store_target<kCount>(a, t, ax, ay, az, pc, pp, steps);
+    store_target<kCount>(a, t, axy.x, axy.y, az, pc, pp, steps);
 }
 
 template <bool kCount, bool kFast>
