@@ -794,8 +794,8 @@ def test_fp32_fma_rate_is_within_the_pipes_nominal_range(tt):
 # ---------------------------------------------------------------------------
 # the radix passes under skewed digits: every key equal (one digit per pass,
 # every tile's whole count in one bin), a few distinct points, keys sharing
-# their high digits, sizes on the 4096-key tile edges, and both kinds of
-# tiles; the tree (keys, permutation, nodes, moments) bit-exact against the
+# their high digits, sizes on the 4096-key tile edges, and every tile size;
+# the tree (keys, permutation, nodes, moments) bit-exact against the
 # oracle
 # ---------------------------------------------------------------------------
 def _sort_stress(name):
@@ -816,8 +816,10 @@ def _sort_stress(name):
 
 @pytest.mark.parametrize("name", ["all_equal_20000", "seven_points_50000", "tight_clump_40961",
                                   "plummer_8191", "plummer_8192", "plummer_12289", "plummer_16385",
-                                  # 8192-key tiles (above 622 592 keys)
-                                  "all_equal_700000", "seven_points_655361", "plummer_622593"])
+                                  # larger tiles above 512 keys per SM thread (622 592 keys on
+                                  # 152 SMs): 5120-key tiles, then 6144, then 8192
+                                  "all_equal_700000", "seven_points_655361", "plummer_622593",
+                                  "plummer_800001", "seven_points_1100000"])
 def test_sort_stress_tree_bit_exact(tt, name):
     pos, mass = _sort_stress(name)
     T = oracle.Tree(pos, mass, 32)

@@ -12,18 +12,20 @@
 // 512-bin histograms), so every pass is a single launch in the manner of the
 // published "Onesweep" radix sort (Adinets and Merrill, 2022) with its
 // decoupled look-back (Merrill and Garland, 2016): a block takes the next
-// tile (4096 keys, or 8192 above 622 592 keys) by ticket, counts its
+// tile (4096 to 8192 keys, sized to the SM count) by ticket, counts its
 // digits, publishes the counts, and adds up the counts of the tiles before
 // it by reading their published words backwards until it meets a tile that
 // has already published its inclusive prefix. A block only ever waits for
 // tiles with smaller tickets, which are already running, so every wait
 // ends; each is still bounded, and a wait that runs out flags an internal
 // error instead of spinning on. The tile is then ranked (each warp walks a
-// contiguous span of 256 or 512 keys, 32 keys at a time, finding the lanes
+// contiguous span of 256 to 512 keys, 32 keys at a time, finding the lanes
 // with equal digits by one vote per digit bit), put in digit order in shared
 // memory, and each digit's run is written to its global slot with
 // consecutive threads on consecutive addresses.
 #include <stdlib.h>
+
+#include <type_traits>
 
 #include <cuda/atomic>
 
@@ -40,12 +42,15 @@ constexpr int kPasses = 7;                      // 7 x 9 = 63 key bits
 constexpr int kBinsPerThread = kBins / kThreads;
 
 // One pass's tile: kItems keys per lane, so kThreads * kItems keys per block
-// and a contiguous span of 32 * kItems keys per warp. 4096-key tiles while
-// there are no more tiles than the 152 SMs, 8192-key tiles beyond (half the
-// tiles, so a shorter look-back chain and one block per SM where 4096-key
-// tiles would double up). Measured sort times: 0.080 vs 0.102 ms at 524 288
-// keys (128 tiles of 4096), 0.123 vs 0.107 ms at 786 432, 0.129 vs 0.111 ms
-// at 1M.
+// and a contiguous span of 32 * kItems keys per warp. A pass is a chain of
+// latencies inside each tile (load, rank, look-back, place, write), so the
+// fastest tiling is the smallest tile that still fills whole waves of one
+// block per SM: kItems is the smallest even count in [8, 16] for which the
+// tiles fill no more than the waves that 16 would need. (Up to 622 592 keys
+// on 152 SMs that is 8: 4096-key tiles, two blocks per SM.) Measured at
+// 1M: 0.106 ms with 7168-key tiles (147 tiles on 152 SMs) against 0.111
+// with 8192 (128 tiles) and 0.129 with 4096; at 2M 0.192 (293 tiles, two
+// waves) against 0.201 (256).
 template <int kItemsT>
 struct Tiling {
     static constexpr int kItems = kItemsT;
@@ -57,9 +62,8 @@ struct Tiling {
     static constexpr int kRanksPerWord = 32 / kRankBits;
     static constexpr uint32_t kRankMask = (1u << kRankBits) - 1u;
 };
-constexpr int kSmallTileItems = 8;   // 4096-key tiles
-constexpr int kLargeTileItems = 16;  // 8192-key tiles
-constexpr int64_t kLargeTileMinN = 152 * 4096 + 1;
+constexpr int kMinTileItems = 8;    // 4096-key tiles
+constexpr int kMaxTileItems = 16;   // 8192-key tiles
 
 // Control words of one sort, cleared before the key kernel: the digit counts
 // of every pass, then one tile ticket per pass.
@@ -538,28 +542,61 @@ k_radix_sort_small(const uint64_t *__restrict__ kin, uint64_t *__restrict__ kout
 
 }  // namespace
 
+// The tile sizes a pass may use, one instantiation each.
+template <int kItems>
+void opt_in_pass()
+{
+    cudaFuncSetAttribute(k_onesweep<kItems>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(PassSmem<kItems>));
+}
+
 void prepare_sort()
 {
     static std::atomic<bool> configured[64];  // the opt-in is set once per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !configured[dev].load()) {
-        cudaFuncSetAttribute(k_onesweep<kSmallTileItems>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(PassSmem<kSmallTileItems>));
-        cudaFuncSetAttribute(k_onesweep<kLargeTileItems>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(PassSmem<kLargeTileItems>));
+        opt_in_pass<8>();
+        opt_in_pass<10>();
+        opt_in_pass<12>();
+        opt_in_pass<14>();
+        opt_in_pass<16>();
         cudaFuncSetAttribute(k_radix_sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(SmallSortSmem));
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
 }
 
-static bool large_tiles(int64_t n) { return n >= kLargeTileMinN; }
+// SMs of the current device (read once per device).
+static int sm_count()
+{
+    static std::atomic<int> sms[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && sms[dev].load() > 0) return sms[dev].load();
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+        cudaGetLastError();
+        v = 1;
+    }
+    if (dev >= 0 && dev < 64) sms[dev] = v;
+    return v;
+}
+
+// Keys per lane of a pass over n keys (see Tiling).
+static int tile_items(int64_t n)
+{
+    const int64_t per_wave = (int64_t)kThreads * sm_count();  // keys per item of a wave
+    const int64_t waves = (n + per_wave * kMaxTileItems - 1) / (per_wave * kMaxTileItems);
+    int64_t items = (n + per_wave * waves - 1) / (per_wave * waves);
+    items += items & 1;
+    return (int)(items < kMinTileItems ? kMinTileItems : items > kMaxTileItems ? kMaxTileItems : items);
+}
 
 // Tiles of the passes for n keys (more than the single-block size).
 static int pass_tiles(int64_t n)
 {
-    const int tile = large_tiles(n) ? Tiling<kLargeTileItems>::kTile : Tiling<kSmallTileItems>::kTile;
+    const int64_t tile = (int64_t)kThreads * tile_items(n);
     return (int)((n + tile - 1) / tile);
 }
 
@@ -600,19 +637,24 @@ void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint
     const bool stalled = stall && stall[0] == '1';
     uint64_t *kin = b.keys_a, *kout = b.keys_b;
     uint32_t *vin = b.idx_a, *vout = b.idx_b;
+    const int items = tile_items(b.n);
     for (int p = 0; p < kPasses; ++p) {
         uint32_t *look = b.sort_look + (p & 1) * look_words;
         uint32_t *look_next = p + 1 < kPasses ? b.sort_look + ((p + 1) & 1) * look_words : nullptr;
-        if (large_tiles(b.n))
-            k_onesweep<kLargeTileItems><<<tiles, kThreads, sizeof(PassSmem<kLargeTileItems>), st>>>(
+        auto pass = [&](auto itag) {
+            constexpr int I = decltype(itag)::value;
+            k_onesweep<I><<<tiles, kThreads, sizeof(PassSmem<I>), st>>>(
                 kin, vin, kout, vout, b.n, p, b.sort_ctl + p * kBins, b.sort_ctl + kCtlCounts + p,
                 look, look_next, tiles, stalled && p == 0 ? 0 : -1,
                 stalled ? kTestLookSpins : kLookSpins, &b.params->status);
-        else
-            k_onesweep<kSmallTileItems><<<tiles, kThreads, sizeof(PassSmem<kSmallTileItems>), st>>>(
-                kin, vin, kout, vout, b.n, p, b.sort_ctl + p * kBins, b.sort_ctl + kCtlCounts + p,
-                look, look_next, tiles, stalled && p == 0 ? 0 : -1,
-                stalled ? kTestLookSpins : kLookSpins, &b.params->status);
+        };
+        switch (items) {
+        case 8: pass(std::integral_constant<int, 8>{}); break;
+        case 10: pass(std::integral_constant<int, 10>{}); break;
+        case 12: pass(std::integral_constant<int, 12>{}); break;
+        case 14: pass(std::integral_constant<int, 14>{}); break;
+        default: pass(std::integral_constant<int, 16>{}); break;
+        }
         g_launches += 1;
         uint64_t *tk = kin;
         kin = kout;
@@ -629,7 +671,7 @@ void launch_sort(const Buffers &b, cudaStream_t st, uint64_t **keys_sorted, uint
 // the size only grows with n, as the workspace assumes).
 int64_t sort_look_words(int64_t n)
 {
-    constexpr int tile = Tiling<kSmallTileItems>::kTile;
+    constexpr int tile = Tiling<kMinTileItems>::kTile;
     return 2 * ((n + tile - 1) / tile) * kBins;
 }
 
