@@ -79,42 +79,85 @@ k_build_levels(const uint64_t *__restrict__ K, int64_t n, int32_t cap,
 // found by k_build_levels, every later one's is the node before it: the
 // cells starting at one position are nested). The cells' ends come from
 // k_build_ends, one node per thread, so no thread walks a chain of searches.
+// A thread takes four consecutive positions and reads each per-position
+// array with one load (4 bytes of counts, 4 of levels, 16 of scan values and
+// of parent-cell starts), then the parent cells' entries of all four at once:
+// two rounds of independent loads instead of a chain per position.
+constexpr int kEmitPositions = 4;
+
 __global__ void __launch_bounds__(kThreads)
 k_build_emit(int64_t n, const int8_t *__restrict__ lev_d, const uint8_t *__restrict__ ncount,
              const int32_t *__restrict__ pstart, const uint32_t *__restrict__ node_start,
              int64_t max_nodes, int4 *__restrict__ meta, int32_t *__restrict__ parent,
              DeviceParams *P)
 {
-    if (P->status & kStatusInternal) return;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
+    // warp-uniform exit (the warp's lanes meet in a reduction below)
+    if (__shfl_sync(0xffffffffu, P->status, 0) & kStatusInternal) return;
+    const int64_t i0 = kEmitPositions * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
     const uint32_t total = node_start[n];
-    if (i == 0) {
+    if (i0 == 0) {
         P->num_nodes = (int)total;
         if ((int64_t)total > max_nodes) atomicOr(&P->status, kStatusNodeBound);
     }
-    const int cnt = ncount[i];
-    if (cnt == 0 || (int64_t)total > max_nodes) return;
-    const int D = lev_d[i];
-    const int first_level = (i == 0) ? 0 : D + 1;
-    const uint32_t base = node_start[i];
-    int32_t par = -1;
-    if (i > 0) {
-        const int64_t s = pstart[i];
-        const int s_first_level = (s == 0) ? 0 : lev_d[s] + 1;
-        par = (int32_t)(node_start[s] + (uint32_t)(D - s_first_level));
-        if (par < 0 || par >= (int32_t)base) {  // a parent precedes its children
-            atomicOr(&P->status, kStatusInternal);
-            return;
+    int cnt[kEmitPositions] = {}, D[kEmitPositions] = {}, s[kEmitPositions] = {};
+    uint32_t base[kEmitPositions] = {};
+    if (i0 < n && (int64_t)total <= max_nodes) {
+        if (i0 + kEmitPositions <= n) {  // the buffers are 256-byte aligned, i0 a multiple of 4
+            const uint32_t c4 = *reinterpret_cast<const uint32_t *>(ncount + i0);
+            const uint32_t d4 = *reinterpret_cast<const uint32_t *>(lev_d + i0);
+            const uint4 b4 = *reinterpret_cast<const uint4 *>(node_start + i0);
+            const int4 s4 = *reinterpret_cast<const int4 *>(pstart + i0);
+#pragma unroll
+            for (int j = 0; j < kEmitPositions; ++j) {
+                cnt[j] = (int)((c4 >> (8 * j)) & 0xffu);
+                D[j] = (int)(int8_t)((d4 >> (8 * j)) & 0xffu);
+            }
+            base[0] = b4.x; base[1] = b4.y; base[2] = b4.z; base[3] = b4.w;
+            s[0] = s4.x; s[1] = s4.y; s[2] = s4.z; s[3] = s4.w;
+        } else {
+            for (int j = 0; j < kEmitPositions && i0 + j < n; ++j) {
+                cnt[j] = ncount[i0 + j];
+                D[j] = lev_d[i0 + j];
+                base[j] = node_start[i0 + j];
+                s[j] = pstart[i0 + j];
+            }
         }
     }
-    for (int j = 0; j < cnt; ++j) {
-        const int64_t k = (int64_t)base + j;
-        meta[k] = make_int4(0, (int)i, 0, first_level + j);  // escape and count: k_build_ends
-        parent[k] = par;
-        par = (int32_t)k;
+    // the parent cell of each position's first node: its first node and level
+    int s_level[kEmitPositions] = {};
+    uint32_t s_base[kEmitPositions] = {};
+#pragma unroll
+    for (int j = 0; j < kEmitPositions; ++j) {
+        if (cnt[j] > 0 && i0 + j > 0) {
+            s_level[j] = (s[j] == 0) ? 0 : lev_d[s[j]] + 1;
+            s_base[j] = node_start[s[j]];
+        }
     }
-    atomicMax(&P->depth, first_level + cnt - 1);
+    int deepest = -1;  // the deepest node of these positions, for the tree depth
+#pragma unroll
+    for (int j = 0; j < kEmitPositions; ++j) {
+        if (cnt[j] == 0) continue;
+        const int64_t i = i0 + j;
+        const int first_level = (i == 0) ? 0 : D[j] + 1;
+        int32_t par = -1;
+        if (i > 0) {
+            par = (int32_t)(s_base[j] + (uint32_t)(D[j] - s_level[j]));
+            if (par < 0 || par >= (int32_t)base[j]) {  // a parent precedes its children
+                atomicOr(&P->status, kStatusInternal);
+                continue;
+            }
+        }
+        for (int l = 0; l < cnt[j]; ++l) {
+            const int64_t k = (int64_t)base[j] + l;
+            meta[k] = make_int4(0, (int)i, 0, first_level + l);  // escape and count: k_build_ends
+            parent[k] = par;
+            par = (int32_t)k;
+        }
+        deepest = max(deepest, first_level + cnt[j] - 1);
+    }
+    // one atomic per warp for the depth, not one per node-starting position
+    deepest = __reduce_max_sync(0xffffffffu, deepest);
+    if ((threadIdx.x & 31) == 0 && deepest >= 0) atomicMax(&P->depth, deepest);
 }
 
 __device__ __forceinline__ void node_end(const uint64_t *__restrict__ K, int64_t n,
@@ -323,7 +366,7 @@ void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &
     g_launches += 1;
     // node_start = exclusive scan of ncount over n + 1 entries
     launch_scan_u8(b.ncount, b.node_start, b.n + 1, b.scan_partial, st);
-    k_build_emit<<<ceil_div(b.n, kThreads), kThreads, 0, st>>>(
+    k_build_emit<<<ceil_div(b.n, (int64_t)kThreads * kEmitPositions), kThreads, 0, st>>>(
         b.n, b.lev_d, b.ncount, b.pstart, b.node_start, b.max_nodes, b.meta, b.parent, b.params);
     k_build_ends<<<node_grid(b), kThreads, 0, st>>>(keys_sorted, b.n, b.node_start, b.max_nodes,
                                                    leaf_cap, b.meta, b.wnode, b.arrive, b.params);
