@@ -288,7 +288,7 @@ void run_tree(Workspace &w, const float *pos, const float *mass, int32_t cap, cu
     record_event(w.ev[EV_GATHER], st);
     launch_build(*keys_sorted, cap, b, st);
     record_event(w.ev[EV_BUILD], st);
-    launch_moments(cap, b, st);
+    launch_moments(*keys_sorted, cap, b, st);
     record_event(w.ev[EV_MOMENTS], st);
 }
 

@@ -31,6 +31,15 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// The child table: for every node, its children's indices by octant (-1
+// where the octant holds no child), so that the moments climb reads a
+// node's children at once instead of following their escape indices one by
+// one. It takes 32 bytes per node and lives in the radix key buffer the
+// sort did not leave its result in (8 bytes per particle), so it is used
+// when the tree has at most n / 4 nodes (a leaf capacity of 32 gives about
+// n / 8); larger trees climb by the escape indices.
+__device__ __forceinline__ bool child_table_fits(int64_t nodes, int64_t n) { return 4 * nodes <= n; }
+
 // Per position: D (levels shared with the previous key), the number of
 // nodes starting here (from D and W, the levels shared with the key leaf_cap
 // ahead), and the start of the parent cell of the first of them.
@@ -89,7 +98,7 @@ __global__ void __launch_bounds__(kThreads)
 k_build_emit(int64_t n, const int8_t *__restrict__ lev_d, const uint8_t *__restrict__ ncount,
              const int32_t *__restrict__ pstart, const uint32_t *__restrict__ node_start,
              int64_t max_nodes, int4 *__restrict__ meta, int32_t *__restrict__ parent,
-             DeviceParams *P)
+             int4 *__restrict__ ctab, DeviceParams *P)
 {
     // warp-uniform exit (the warp's lanes meet in a reduction below)
     if (__shfl_sync(0xffffffffu, P->status, 0) & kStatusInternal) return;
@@ -133,6 +142,7 @@ k_build_emit(int64_t n, const int8_t *__restrict__ lev_d, const uint8_t *__restr
             s_base[j] = node_start[s[j]];
         }
     }
+    const bool table = child_table_fits(total, n);
     int deepest = -1;  // the deepest node of these positions, for the tree depth
 #pragma unroll
     for (int j = 0; j < kEmitPositions; ++j) {
@@ -151,6 +161,10 @@ k_build_emit(int64_t n, const int8_t *__restrict__ lev_d, const uint8_t *__restr
             const int64_t k = (int64_t)base[j] + l;
             meta[k] = make_int4(0, (int)i, 0, first_level + l);  // escape and count: k_build_ends
             parent[k] = par;
+            if (table) {  // no children yet: k_build_ends enters them
+                ctab[2 * k] = make_int4(-1, -1, -1, -1);
+                ctab[2 * k + 1] = make_int4(-1, -1, -1, -1);
+            }
             par = (int32_t)k;
         }
         deepest = max(deepest, first_level + cnt[j] - 1);
@@ -164,6 +178,7 @@ __device__ __forceinline__ void node_end(const uint64_t *__restrict__ K, int64_t
                                          const uint32_t *__restrict__ node_start, int64_t total,
                                          int32_t leaf_cap, int4 *__restrict__ meta,
                                          WalkNode *__restrict__ wnode, int32_t *__restrict__ arrive,
+                                         const int32_t *__restrict__ parent, int32_t *__restrict__ ctab,
                                          DeviceParams *P, int64_t k)
 {
     const int4 m = meta[k];
@@ -195,6 +210,13 @@ __device__ __forceinline__ void node_end(const uint64_t *__restrict__ K, int64_t
     const bool leaf = count <= leaf_cap || L == kLevels;
     meta[k] = make_int4(esc, (int)i, count, L);
     arrive[k] = 0;
+    // this node in its parent's row of the child table, under its octant
+    // (the parent's cell split by the level-L digit; children in key order
+    // are children in octant order)
+    if (ctab && L > 0) {
+        const int32_t par = parent[k];
+        if (par >= 0 && par < k) ctab[8 * (int64_t)par + (int)((K[i] >> (3 * (kLevels - L))) & 7u)] = (int32_t)k;
+    }
     wnode[k].w = make_int4(esc, leaf ? esc : (int)k + 1, leaf ? count : 0, __float_as_int(P->s2[L]));
 }
 
@@ -214,7 +236,8 @@ __device__ __forceinline__ void node_end(const uint64_t *__restrict__ K, int64_t
 __global__ void __launch_bounds__(kThreads)
 k_build_ends(const uint64_t *__restrict__ K, int64_t n, const uint32_t *__restrict__ node_start,
              int64_t max_nodes, int32_t leaf_cap, int4 *__restrict__ meta,
-             WalkNode *__restrict__ wnode, int32_t *__restrict__ arrive, DeviceParams *P)
+             WalkNode *__restrict__ wnode, int32_t *__restrict__ arrive,
+             const int32_t *__restrict__ parent, int32_t *__restrict__ ctab, DeviceParams *P)
 {
     if (P->status & kStatusInternal) return;
     const int64_t total = node_start[n];
@@ -226,8 +249,9 @@ k_build_ends(const uint64_t *__restrict__ K, int64_t n, const uint32_t *__restri
         wnode[total].w = make_int4((int)total, (int)total, 1, 0x7f800000);
         wnode[total].c = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
+    int32_t *table = child_table_fits(total, n) ? ctab : nullptr;
     for (int64_t k = first_k; k < total; k += (int64_t)gridDim.x * blockDim.x)
-        node_end(K, n, node_start, total, leaf_cap, meta, wnode, arrive, P, k);
+        node_end(K, n, node_start, total, leaf_cap, meta, wnode, arrive, parent, table, P, k);
 }
 // A node whose mass is not finite or whose CoM lies at 2^126 or beyond is
 // reported as non-finite: with every coordinate below 2^125 (checked with the
@@ -266,7 +290,8 @@ __device__ __forceinline__ void leaf_and_climb(const float4 *__restrict__ ps, in
                                                const int4 *__restrict__ meta,
                                                const int32_t *__restrict__ parent,
                                                int32_t *__restrict__ arrive, float4 *sums,
-                                               WalkNode *__restrict__ wnode, DeviceParams *P,
+                                               WalkNode *__restrict__ wnode,
+                                               const int4 *__restrict__ ctab, DeviceParams *P,
                                                int total, int64_t k, int4 m)
 {
     if (m.y < 0 || m.z < 0 || (int64_t)m.y + m.z > n) {
@@ -312,6 +337,32 @@ __device__ __forceinline__ void leaf_and_climb(const float4 *__restrict__ ps, in
             atomicOr((int *)&P->status, kStatusInternal);
             return;
         }
+        if (ctab) {  // the children by octant, read at once, summed in octant order
+            const int4 lo = ctab[2 * node], hi = ctab[2 * node + 1];
+            const int ch[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            float4 cs[8];
+#pragma unroll
+            for (int o = 0; o < 8; ++o) {
+                const bool in = ch[o] > node && ch[o] < esc;  // a child lies inside its parent's range
+                if (ch[o] >= 0 && !in) {
+                    atomicOr((int *)&P->status, kStatusInternal);
+                    return;
+                }
+                cs[o] = in ? __ldcg(sums + ch[o]) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int o = 0; o < 8; ++o) {
+                if (ch[o] < 0) continue;
+                M = __fadd_rn(M, cs[o].w);
+                sx = __fadd_rn(sx, cs[o].x);
+                sy = __fadd_rn(sy, cs[o].y);
+                sz = __fadd_rn(sz, cs[o].z);
+            }
+            store_node(node, sx, sy, sz, M, sums, wnode, P);
+            carried = pm.z;
+            node = parent[node];
+            continue;
+        }
         for (int c = (int)node + 1; c < esc;) {
             const float4 s = __ldcg(sums + c);
             M = __fadd_rn(M, s.w);
@@ -335,15 +386,16 @@ __global__ void __launch_bounds__(kThreads)
 k_moments(const float4 *__restrict__ ps, int64_t n, int32_t leaf_cap,
           const int4 *__restrict__ meta, const int32_t *__restrict__ parent,
           int32_t *__restrict__ arrive, float4 *sums, WalkNode *__restrict__ wnode,
-          DeviceParams *P)
+          const int4 *__restrict__ ctab, DeviceParams *P)
 {
     if (P->status & (kStatusNodeBound | kStatusInternal)) return;
     const int total = P->num_nodes;
+    const int4 *table = child_table_fits(total, n) ? ctab : nullptr;
     for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total;
          k += (int64_t)gridDim.x * blockDim.x) {
         const int4 m = meta[k];
         if (m.z <= leaf_cap || m.w == kLevels)  // a leaf
-            leaf_and_climb(ps, n, meta, parent, arrive, sums, wnode, P, total, k, m);
+            leaf_and_climb(ps, n, meta, parent, arrive, sums, wnode, table, P, total, k, m);
     }
 }
 
@@ -358,25 +410,35 @@ static unsigned node_grid(const Buffers &b)
     return want < 152u * 8u ? want : 152u * 8u;
 }
 
+// The child table's storage: the radix key buffer that does not hold the
+// sorted keys (free once the sort is done).
+static void *child_table(const uint64_t *keys_sorted, const Buffers &b)
+{
+    return keys_sorted == b.keys_a ? (void *)b.keys_b : (void *)b.keys_a;
+}
+
 void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b,
                   cudaStream_t st)
 {
+    int4 *ctab = (int4 *)child_table(keys_sorted, b);
     k_build_levels<<<ceil_div(b.n + 1, kThreads), kThreads, 0, st>>>(
         keys_sorted, b.n, leaf_cap, b.lev_d, b.ncount, b.pstart, &b.params->status);
     g_launches += 1;
     // node_start = exclusive scan of ncount over n + 1 entries
     launch_scan_u8(b.ncount, b.node_start, b.n + 1, b.scan_partial, st);
     k_build_emit<<<ceil_div(b.n, (int64_t)kThreads * kEmitPositions), kThreads, 0, st>>>(
-        b.n, b.lev_d, b.ncount, b.pstart, b.node_start, b.max_nodes, b.meta, b.parent, b.params);
+        b.n, b.lev_d, b.ncount, b.pstart, b.node_start, b.max_nodes, b.meta, b.parent, ctab, b.params);
     k_build_ends<<<node_grid(b), kThreads, 0, st>>>(keys_sorted, b.n, b.node_start, b.max_nodes,
-                                                   leaf_cap, b.meta, b.wnode, b.arrive, b.params);
+                                                   leaf_cap, b.meta, b.wnode, b.arrive, b.parent,
+                                                   (int32_t *)ctab, b.params);
     g_launches += 2;
 }
 
-void launch_moments(int32_t leaf_cap, const Buffers &b, cudaStream_t st)
+void launch_moments(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b, cudaStream_t st)
 {
     k_moments<<<node_grid(b), kThreads, 0, st>>>(b.ps, b.n, leaf_cap, b.meta, b.parent, b.arrive,
-                                                b.sums, b.wnode, b.params);
+                                                b.sums, b.wnode, (const int4 *)child_table(keys_sorted, b),
+                                                b.params);
     g_launches += 1;
 }
 

@@ -92,7 +92,10 @@ void launch_gather(const float *pos, const float *mass, const uint32_t *perm, co
                    cudaStream_t st);
 void launch_build(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b,
                   cudaStream_t st);
-void launch_moments(int32_t leaf_cap, const Buffers &b, cudaStream_t st);
+// keys_sorted: the buffer launch_sort left the keys in (the other one holds
+// the moments' child table).
+void launch_moments(const uint64_t *keys_sorted, int32_t leaf_cap, const Buffers &b,
+                    cudaStream_t st);
 // a7 with the a8 scatter fused: results land in the caller's order. Walks
 // the sorted targets [t_begin, t_end) against the whole tree.
 void launch_walk(int traversal, float theta, float eps, const uint32_t *perm, const Buffers &b,

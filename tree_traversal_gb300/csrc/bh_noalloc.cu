@@ -89,7 +89,7 @@ extern "C" int orrery_bh_forces_noalloc(const float *pos_d, const float *mass_d,
     launch_sort(b, st, &keys_sorted, &perm);
     launch_gather(pos_d, mass_d, perm, b, st);
     launch_build(keys_sorted, leaf_cap, b, st);
-    launch_moments(leaf_cap, b, st);
+    launch_moments(keys_sorted, leaf_cap, b, st);
     launch_walk(traversal, theta, eps, perm, b, 0, n, acc_d, interactions_d, visits_d, st);
     int status = 0;
     cudaMemcpyAsync(&status, &b.params->status, sizeof(int), cudaMemcpyDeviceToHost, st);
