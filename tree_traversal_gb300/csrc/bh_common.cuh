@@ -107,7 +107,8 @@ void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *p
                     cudaStream_t st);
 int64_t scan_partial_count(int64_t count);
 int64_t sort_look_words(int64_t n);  // both look-back arrays
-int sort_ctl_words();
+int sort_ctl_words();  // cleared by launch_bbox at the start of every evaluation
+unsigned *bbox_ticket(const Buffers &b);  // the last of them: the bounding box's fold ticket
 void prepare_sort();  // sets the sort kernels' function attributes on this device
 void prepare_walk();  // sets the walk kernels' function attributes on this device
 

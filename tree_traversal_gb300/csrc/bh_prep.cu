@@ -68,51 +68,85 @@ __device__ __forceinline__ void block_fold(float lo[3], float hi[3], float mmax,
     }
 }
 
-// a1, part 1: per-block min / max per axis, max |m| and a non-finite flag.
-__global__ void __launch_bounds__(kBBoxThreads)
-k_bbox_partial(const float *__restrict__ pos, const float *__restrict__ mass, int64_t n,
-               float *__restrict__ partial)
+// Adds particle {x, y, z} of mass m to a thread's running extent.
+__device__ __forceinline__ void extend(float x, float y, float z, float m, float lo[3], float hi[3],
+                                       float &mmax, int &bad)
 {
-    float lo[3] = {INFINITY, INFINITY, INFINITY};
-    float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
-    float mmax = 0.0f;
-    int bad = 0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        float m = __ldg(mass + i);
-        bad |= !isfinite(m);
-        mmax = fmaxf(mmax, fabsf(m));
+    const float v[3] = {x, y, z};
+    bad |= !isfinite(m);
+    mmax = fmaxf(mmax, fabsf(m));
 #pragma unroll
-        for (int a = 0; a < 3; ++a) {
-            float x = __ldg(pos + 3 * i + a);
-            bad |= !(fabsf(x) < 0x1p125f);  // non-finite, or beyond the supported range
-            lo[a] = fminf(lo[a], x);
-            hi[a] = fmaxf(hi[a], x);
-        }
+    for (int a = 0; a < 3; ++a) {
+        bad |= !(fabsf(v[a]) < 0x1p125f);  // non-finite, or beyond the supported range
+        lo[a] = fminf(lo[a], v[a]);
+        hi[a] = fmaxf(hi[a], v[a]);
     }
-    block_fold(lo, hi, mmax, bad, partial + 8 * blockIdx.x);
 }
 
-// a1, part 2: one block folds the partials and derives the cube:
+// a1: per-block min / max per axis, max |m| and a non-finite flag, then the
+// last block to finish folds all blocks' partials and derives the cube:
 // side = max_a (hi_a - lo_a), inv = 2^21 / side, and the per-level squared
 // cell side s2[L] = (side * side) * 2^(-2L) (an exact power-of-two scaling).
-// Also resets the status word, node count and depth of this evaluation.
+// It also resets the status word, node count and depth of this evaluation.
+// A thread reads four particles at a time with 16-byte loads when the
+// arrays allow it. ticket: zero on entry (cleared with the sort's control
+// words before the launch).
 __global__ void __launch_bounds__(kBBoxThreads)
-k_bbox_final(const float *__restrict__ partial, int blocks, DeviceParams *P)
+k_bbox(const float *__restrict__ pos, const float *__restrict__ mass, int64_t n,
+       float *__restrict__ partial, unsigned *ticket, DeviceParams *P)
 {
-    __shared__ float s_out[8];
     float lo[3] = {INFINITY, INFINITY, INFINITY};
     float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
     float mmax = 0.0f;
     int bad = 0;
-    for (int b = threadIdx.x; b < blocks; b += blockDim.x) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const bool vec = ((reinterpret_cast<uintptr_t>(pos) | reinterpret_cast<uintptr_t>(mass)) & 15u) == 0;
+    int64_t done = 0;  // particles covered by the four-at-a-time loop
+    if (vec) {
+        const float4 *p4 = reinterpret_cast<const float4 *>(pos);
+        const float4 *m4 = reinterpret_cast<const float4 *>(mass);
+        const int64_t quads = n / 4;
+        for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += stride) {
+            const float4 a = __ldg(p4 + 3 * q), b = __ldg(p4 + 3 * q + 1), c = __ldg(p4 + 3 * q + 2);
+            const float4 m = __ldg(m4 + q);
+            extend(a.x, a.y, a.z, m.x, lo, hi, mmax, bad);
+            extend(a.w, b.x, b.y, m.y, lo, hi, mmax, bad);
+            extend(b.z, b.w, c.x, m.z, lo, hi, mmax, bad);
+            extend(c.y, c.z, c.w, m.w, lo, hi, mmax, bad);
+        }
+        done = 4 * quads;
+    }
+    for (int64_t i = done + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+        extend(__ldg(pos + 3 * i), __ldg(pos + 3 * i + 1), __ldg(pos + 3 * i + 2), __ldg(mass + i), lo, hi,
+               mmax, bad);
+    block_fold(lo, hi, mmax, bad, partial + 8 * blockIdx.x);
+
+    // the last block: fold the partials (they were written before each
+    // block's ticket, and are read past L1)
+    __shared__ bool s_last;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    __shared__ float s_out[8];
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        lo[a] = INFINITY;
+        hi[a] = -INFINITY;
+    }
+    mmax = 0.0f;
+    bad = 0;
+    for (int b = threadIdx.x; b < (int)gridDim.x; b += blockDim.x) {
         const float *o = partial + 8 * b;
         for (int a = 0; a < 3; ++a) {
-            lo[a] = fminf(lo[a], o[a]);
-            hi[a] = fmaxf(hi[a], o[3 + a]);
+            lo[a] = fminf(lo[a], __ldcg(o + a));
+            hi[a] = fmaxf(hi[a], __ldcg(o + 3 + a));
         }
-        bad |= (o[6] != 0.0f);
-        mmax = fmaxf(mmax, o[7]);
+        bad |= (__ldcg(o + 6) != 0.0f);
+        mmax = fmaxf(mmax, __ldcg(o + 7));
     }
     block_fold(lo, hi, mmax, bad, s_out);
     __syncthreads();
@@ -138,7 +172,9 @@ k_bbox_final(const float *__restrict__ partial, int blocks, DeviceParams *P)
     P->depth = 0;
 }
 
-// a4: sorted particles {x, y, z, m}.
+// a4: sorted particles {x, y, z, m}. (Four slots per thread, with the
+// sixteen gathers issued together, measured the same: the gather is bound by
+// its traffic, not by load latency.)
 __global__ void __launch_bounds__(256)
 k_gather(const float *__restrict__ pos, const float *__restrict__ mass,
          const uint32_t *__restrict__ perm, int64_t n, float4 *__restrict__ ps, int *status)
@@ -269,11 +305,14 @@ void launch_scan_u8(const uint8_t *in, uint32_t *out, int64_t count, uint32_t *p
     scan_exclusive<uint8_t>(in, out, count, partial, st);
 }
 
+// Clears the sort's control words (and with them the fold ticket), then
+// finds the cube.
 void launch_bbox(const float *pos, const float *mass, const Buffers &b, cudaStream_t st)
 {
-    k_bbox_partial<<<b.bbox_blocks, kBBoxThreads, 0, st>>>(pos, mass, b.n, b.bbox_partial);
-    k_bbox_final<<<1, kBBoxThreads, 0, st>>>(b.bbox_partial, b.bbox_blocks, b.params);
-    g_launches += 2;
+    cudaMemsetAsync(b.sort_ctl, 0, sizeof(uint32_t) * (size_t)sort_ctl_words(), st);
+    k_bbox<<<b.bbox_blocks, kBBoxThreads, 0, st>>>(pos, mass, b.n, b.bbox_partial, bbox_ticket(b),
+                                                   b.params);
+    g_launches += 1;
 }
 
 void launch_gather(const float *pos, const float *mass, const uint32_t *perm, const Buffers &b,

@@ -65,10 +65,11 @@ struct Tiling {
 constexpr int kMinTileItems = 8;    // 4096-key tiles
 constexpr int kMaxTileItems = 16;   // 8192-key tiles
 
-// Control words of one sort, cleared before the key kernel: the digit counts
-// of every pass, then one tile ticket per pass.
+// Control words of one evaluation, cleared before the bounding box: the
+// digit counts of every pass, one tile ticket per pass, and the bounding
+// box's fold ticket.
 constexpr int kCtlCounts = kPasses * kBins;
-constexpr int kCtlWords = kCtlCounts + 8;
+constexpr int kCtlWords = kCtlCounts + kPasses + 1;
 
 // A look-back word: bit 31 set = the inclusive count of the digit over this
 // tile and all before it (at most 2^30, the largest n); bit 30 set = this
@@ -609,7 +610,6 @@ void launch_morton(const float *pos, const Buffers &b, cudaStream_t st)
         g_launches += 1;
         return;
     }
-    cudaMemsetAsync(b.sort_ctl, 0, sizeof(uint32_t) * kCtlWords, st);
     int64_t blocks = ((int64_t)b.n + kCountThreads * kCountKeysPerThread - 1) /
                      (kCountThreads * kCountKeysPerThread);
     if (blocks > kCountMaxBlocks) blocks = kCountMaxBlocks;
@@ -676,5 +676,7 @@ int64_t sort_look_words(int64_t n)
 }
 
 int sort_ctl_words() { return kCtlWords; }
+
+unsigned *bbox_ticket(const Buffers &b) { return b.sort_ctl + kCtlCounts + kPasses; }
 
 }  // namespace obh
