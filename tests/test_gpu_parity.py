@@ -19,6 +19,11 @@ Bars:
 Sizes span several radix tiles and scan tiles (2048 entries each) with
 ragged tails; the full-size workloads (1M Plummer, two 1M spheres swept over
 theta) are compared over the whole tree and on sampled warps of targets.
+The moments take two paths: trees of at most n / 4 nodes read each node's
+children from the octant child table (every leaf-32 case here), larger
+trees follow the escape indices (ragged_5003_cap7, clump_cap8,
+grid_ties_cap4, edge_8193_cap3, tiny_33_cap1, the duplicate cases); both
+are held to the same bit-exact moments.
 """
 from __future__ import annotations
 
