@@ -66,9 +66,9 @@ k_build_levels(const uint64_t *__restrict__ K, int64_t n, int32_t cap,
         // start of the level-D cell holding key[i-1] and key[i]: the first
         // position whose key is >= key with its low 3(21-D) bits cleared
         const uint64_t prefix = key & ~((1ull << (3 * (kLevels - D))) - 1ull);
-        int64_t lo = 0, hi = i;
+        uint32_t lo = 0, hi = (uint32_t)i;  // n < 2^31: 32-bit indices (fewer instructions per step)
         while (lo < hi) {
-            int64_t mid = (lo + hi) >> 1;
+            const uint32_t mid = (lo + hi) >> 1;
             if (K[mid] < prefix)
                 lo = mid + 1;
             else
@@ -191,9 +191,9 @@ __device__ __forceinline__ void node_end(const uint64_t *__restrict__ K, int64_t
     int64_t end = n;
     if (L > 0) {
         const uint64_t upper = K[i] | ((1ull << (3 * (kLevels - L))) - 1ull);
-        int64_t lo = i + 1, hi = n;
+        uint32_t lo = (uint32_t)i + 1, hi = (uint32_t)n;  // n < 2^31: 32-bit indices
         while (lo < hi) {
-            const int64_t mid = (lo + hi) >> 1;
+            const uint32_t mid = (lo + hi) >> 1;
             if (K[mid] <= upper)
                 lo = mid + 1;
             else
