@@ -307,6 +307,31 @@ def test_host_entry_point_matches_device(tt):
     assert np.array_equal(a2.view(np.uint32), acc.cpu().numpy().view(np.uint32))
 
 
+def test_host_entry_point_repeated_into_page_locked_outputs(tt):
+    """With every output page-locked nothing is copied after the walk, so a
+    repeated call replays the captured evaluation (from the second repeat
+    on); each call copies its inputs in afresh, so new input values in the
+    same buffers give the device entry point's bits for those values."""
+    pos, mass, cap, T = case("plummer_16384")
+    h_pos = torch.from_numpy(pos.copy()).pin_memory()
+    h_mass = torch.from_numpy(mass.copy()).pin_memory()
+    out = (torch.empty((T.n, 3)).pin_memory(), torch.empty((T.n, 2), dtype=torch.int32).pin_memory(),
+           torch.empty(T.n, dtype=torch.int32).pin_memory())
+    for call in range(5):
+        if call == 3:  # new values in the same page-locked input buffers
+            h_pos.mul_(1.25)
+            h_mass.mul_(0.5)
+        acc, inter, vis = tt.bh_forces(h_pos.cuda(), h_mass.cuda(), 0.5, EPS, cap, "coherent64",
+                                       fast_term=True)
+        out[0].zero_()
+        tt.bh_forces_host(h_pos, h_mass, 0.5, EPS, cap, "coherent64", out=out, fast_term=True)
+        assert np.array_equal(out[0].numpy().view(np.uint32), acc.cpu().numpy().view(np.uint32)), call
+        assert np.array_equal(out[1].numpy(), inter.cpu().numpy()), call
+        assert np.array_equal(out[2].numpy(), vis.cpu().numpy()), call
+        t = tt.last_timings()
+        assert t["h2d_ms"] >= 0 and t["d2h_ms"] == 0.0 and t["total_ms"] >= t["walk_ms"], (call, t)
+
+
 def test_host_entry_point_mixed_page_locked_and_pageable_outputs(tt):
     """Page-locked outputs are written by the walk directly, pageable ones
     copied after it: any mix gives the device entry point's bits."""
